@@ -1,0 +1,372 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU reference for DeepSeek-V4 sparse-MLA decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file; it exists so that tests, the smoke check and the benchmark's CPU
+ * baseline can check the GPU path against an independent restatement of what
+ * the path computes.  It shares no code with the CUDA library.
+ *
+ * Sources (the vLLM pull-request summaries the method is taken from):
+ *  - combine: "[ROCm] [DSv4] [Perf] Support DeepSeek v4 MTP" (vllm #43385),
+ *    section "关键源码片段 / rocm.py", the _combine_topk_swa_indices_kernel:
+ *    per token, valid top-k entries first (in input order), then the sliding
+ *    window [pos - swa_len + 1, pos] ascending, swa_len = min(pos + 1, W),
+ *    pos = seq_len - query_len + i; an entry is valid when 0 <= idx < N.
+ *    Readings taken here (the pages index two different cache regions, this
+ *    path one): entries > pos, entries inside the window and repeats (all but
+ *    the first occurrence) are dropped, and the survivors are compacted.
+ *  - dequant: "feat: add DeepSeek-V4 XPU attention decode path" (vllm #42953),
+ *    section "xpu_sparse_decode_fp8.py", _dequant_gather_slots_kernel:
+ *    value = fp8_e4m3 * exp2(ue8m0 - 127); a negative slot contributes zeros;
+ *    block_idx = slot // block_size, pos_in_block = slot % block_size; the
+ *    BF16 RoPE part is copied as stored.
+ *  - logical -> physical: "Enable DeepSeek V4 and GLM-5.1 on SM120"
+ *    (vllm #43477), section "flashinfer_mla_sparse_sm120.py",
+ *    triton_convert_req_index_to_global_index(req_id_per_token, block_table, ...).
+ *  - attention: the same page's forward_mqa: output [T, h, kv_lora_rank=512]
+ *    over MQA keys (one KV head, V = the 512-d latent), sinks supported
+ *    (flashinfer_sparse.py, supports_sink).  Written here as its plain
+ *    definition: s_j = scale * q . k_j over 576 dims; with an optional sink
+ *    logit sigma (in the same units as s), Z = sum_j e^{s_j} + e^{sigma},
+ *    lse = ln Z, out = sum_j e^{s_j - lse} v_j.
+ *  - merge of split partial results: the log-sum-exp combination, written out
+ *    from its definition (not on the pages; needed when one token's keys are
+ *    split over several workers).
+ *
+ * Cache entry layout (656 bytes per token, this library's own layout):
+ *   [0,512) E4M3FN latent codes, [512,640) 64 x BF16 rope (little endian),
+ *   [640,644) four UE8M0 scale bytes (byte b scales latent dims [128b,128b+128)),
+ *   [644,656) padding.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_ENTRY_BYTES 656
+#define OR_LATENT 512
+#define OR_ROPE 64
+#define OR_DIM 576
+#define OR_ROPE_OFF 512
+#define OR_SCALE_OFF 640
+#define OR_SCALE_BLOCK 128
+
+/* OCP FP8 E4M3FN: 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent 0
+ * is subnormal (m/8 * 2^-6); S.1111.111 is NaN; there are no infinities. */
+double oracle_e4m3_to_double(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* UE8M0: an unsigned 8-bit exponent, value 2^(e - 127); 0xFF is NaN. */
+double oracle_ue8m0_to_double(uint8_t e)
+{
+    if (e == 0xFF)
+        return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+/* BF16: the upper 16 bits of an IEEE binary32. */
+double oracle_bf16_to_double(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* One cache entry -> the 576-d key (512 latent then 64 rope). */
+void oracle_dequant_entry(const uint8_t *entry, double *k)
+{
+    for (int d = 0; d < OR_LATENT; ++d) {
+        double scale = oracle_ue8m0_to_double(entry[OR_SCALE_OFF + d / OR_SCALE_BLOCK]);
+        k[d] = oracle_e4m3_to_double(entry[d]) * scale;
+    }
+    for (int i = 0; i < OR_ROPE; ++i) {
+        uint16_t h = (uint16_t)entry[OR_ROPE_OFF + 2 * i] | (uint16_t)((uint16_t)entry[OR_ROPE_OFF + 2 * i + 1] << 8);
+        k[OR_LATENT + i] = oracle_bf16_to_double(h);
+    }
+}
+
+/* Combined index list of one token.  Returns its length L; row[0..L) holds
+ * the kept top-k entries then the window, row[L..width) is -1. */
+int oracle_combine_token(const int32_t *topk_row, int32_t n_topk, int32_t seq_len, int32_t window,
+                         int32_t *row, int32_t width)
+{
+    int32_t pos = seq_len - 1;
+    int32_t win_lo = pos - window + 1;
+    if (win_lo < 0)
+        win_lo = 0;
+    int32_t L = 0;
+    for (int32_t i = 0; i < n_topk; ++i) {
+        int32_t v = topk_row[i];
+        if (v < 0 || v > pos)
+            continue;                 /* invalid or not causal */
+        if (v >= win_lo)
+            continue;                 /* already covered by the window */
+        int dup = 0;
+        for (int32_t j = 0; j < L; ++j) {
+            if (row[j] == v) {
+                dup = 1;
+                break;
+            }
+        }
+        if (!dup)
+            row[L++] = v;
+    }
+    for (int32_t p = win_lo; p <= pos; ++p)
+        row[L++] = p;
+    for (int32_t j = L; j < width; ++j)
+        row[j] = -1;
+    return L;
+}
+
+/* Batched combine; returns 0, or -1 when a row would not fit in `width`. */
+int oracle_combine(const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width, const int32_t *topk_lens,
+                   const int32_t *seq_lens, int32_t num_tokens, int32_t window, int32_t *combined,
+                   int64_t combined_stride, int32_t combined_width, int32_t *combined_lens)
+{
+    int32_t *tmp = (int32_t *)malloc(sizeof(int32_t) * ((size_t)topk_width + (size_t)(window > 0 ? window : 0) + 1));
+    if (!tmp)
+        return -1;
+    int rc = 0;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int32_t n = topk_lens ? topk_lens[t] : topk_width;
+        if (n < 0)
+            n = 0;
+        if (n > topk_width)
+            n = topk_width;
+        int32_t L = oracle_combine_token(topk_idx + (int64_t)t * topk_stride, n, seq_lens[t], window, tmp,
+                                         topk_width + (window > 0 ? window : 0));
+        if (L > combined_width) {
+            rc = -1;
+            L = combined_width;
+        }
+        memcpy(combined + (int64_t)t * combined_stride, tmp, sizeof(int32_t) * (size_t)L);
+        for (int32_t j = L; j < combined_width; ++j)
+            combined[(int64_t)t * combined_stride + j] = -1;
+        combined_lens[t] = L;
+    }
+    free(tmp);
+    return rc;
+}
+
+/* Attention of one head over an explicit key list keys[L][576] (V = first 512 dims).
+ * q is the 576-d query in fp64.  has_sink selects the optional sink logit. */
+void oracle_attend(const double *q, const double *keys, int32_t L, double softmax_scale, int has_sink, double sink,
+                   double *out, double *lse)
+{
+    double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    double m = -INFINITY;
+    for (int32_t j = 0; j < L; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < OR_DIM; ++d)
+            acc += q[d] * keys[(int64_t)j * OR_DIM + d];
+        s[j] = softmax_scale * acc;
+        if (s[j] > m)
+            m = s[j];
+    }
+    if (has_sink && sink > m)
+        m = sink;
+    for (int d = 0; d < OR_LATENT; ++d)
+        out[d] = 0.0;
+    if (m == -INFINITY) {           /* no key and no (finite) sink */
+        *lse = -INFINITY;
+        free(s);
+        return;
+    }
+    double z = 0.0;
+    for (int32_t j = 0; j < L; ++j)
+        z += exp(s[j] - m);
+    if (has_sink)
+        z += exp(sink - m);
+    double l = m + log(z);
+    for (int32_t j = 0; j < L; ++j) {
+        double w = exp(s[j] - l);
+        for (int d = 0; d < OR_LATENT; ++d)
+            out[d] += w * keys[(int64_t)j * OR_DIM + d];
+    }
+    *lse = l;
+    free(s);
+}
+
+/* Merge of S partial results over disjoint key sets, each given as
+ * (lse_c = ln sum_{j in c} e^{s_j}, out_c normalised within c), plus the
+ * optional sink: lse = ln(sum_c e^{lse_c} + e^{sink}), out = sum_c e^{lse_c - lse} out_c. */
+void oracle_merge(int32_t S, const double *lse_parts, const double *out_parts, int has_sink, double sink,
+                  double *out, double *lse)
+{
+    double m = -INFINITY;
+    for (int32_t c = 0; c < S; ++c)
+        if (lse_parts[c] > m)
+            m = lse_parts[c];
+    if (has_sink && sink > m)
+        m = sink;
+    for (int d = 0; d < OR_LATENT; ++d)
+        out[d] = 0.0;
+    if (m == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double z = 0.0;
+    for (int32_t c = 0; c < S; ++c)
+        z += exp(lse_parts[c] - m);
+    if (has_sink)
+        z += exp(sink - m);
+    double l = m + log(z);
+    for (int32_t c = 0; c < S; ++c) {
+        double w = exp(lse_parts[c] - l);
+        if (w == 0.0)
+            continue;
+        for (int d = 0; d < OR_LATENT; ++d)
+            out[d] += w * out_parts[(int64_t)c * OR_LATENT + d];
+    }
+    *lse = l;
+}
+
+typedef struct {
+    const uint16_t *q;
+    int64_t q_token_stride;
+    const uint8_t *kv_cache;
+    int32_t num_blocks, page_block;
+    const int32_t *block_table;
+    int64_t bt_stride;
+    int32_t max_blocks, num_reqs;
+    const int32_t *req_idx;
+    const int32_t *topk_idx;
+    int64_t topk_stride;
+    int32_t topk_width;
+    const int32_t *topk_lens, *seq_lens;
+    int32_t num_tokens, num_heads, window;
+    const float *sink;
+    double softmax_scale;
+    double *out, *lse;
+    const int32_t *tokens;
+    int32_t n_tokens_todo;
+    int32_t worker, n_workers;
+    int64_t bad;
+} decode_job;
+
+static void *decode_worker(void *arg)
+{
+    decode_job *jb = (decode_job *)arg;
+    int32_t cap = jb->topk_width + (jb->window > 0 ? jb->window : 0) + 1;
+    int32_t *list = (int32_t *)malloc(sizeof(int32_t) * (size_t)cap);
+    double *keys = (double *)malloc(sizeof(double) * (size_t)cap * OR_DIM);
+    double qh[OR_DIM];
+    jb->bad = 0;
+    for (int32_t w = jb->worker; w < jb->n_tokens_todo; w += jb->n_workers) {
+        int32_t t = jb->tokens ? jb->tokens[w] : w;
+        int32_t n = jb->topk_lens ? jb->topk_lens[t] : jb->topk_width;
+        if (n < 0)
+            n = 0;
+        if (n > jb->topk_width)
+            n = jb->topk_width;
+        int32_t L = oracle_combine_token(jb->topk_idx + (int64_t)t * jb->topk_stride, n, jb->seq_lens[t],
+                                         jb->window, list, cap);
+        int32_t row = jb->req_idx ? jb->req_idx[t] : t;
+        int32_t nk = 0;
+        for (int32_t j = 0; j < L; ++j) {
+            int32_t idx = list[j];
+            int32_t blk = idx / jb->page_block;
+            int32_t off = idx % jb->page_block;
+            if (row < 0 || row >= jb->num_reqs || blk >= jb->max_blocks) {
+                jb->bad++;
+                continue;
+            }
+            int32_t phys = jb->block_table[(int64_t)row * jb->bt_stride + blk];
+            if (phys < 0 || phys >= jb->num_blocks) {
+                jb->bad++;
+                continue;
+            }
+            int64_t slot = (int64_t)phys * jb->page_block + off;
+            oracle_dequant_entry(jb->kv_cache + slot * OR_ENTRY_BYTES, keys + (int64_t)nk * OR_DIM);
+            nk++;
+        }
+        for (int32_t h = 0; h < jb->num_heads; ++h) {
+            const uint16_t *qp = jb->q + (int64_t)t * jb->q_token_stride + (int64_t)h * OR_DIM;
+            for (int d = 0; d < OR_DIM; ++d)
+                qh[d] = oracle_bf16_to_double(qp[d]);
+            double *o = jb->out + ((int64_t)w * jb->num_heads + h) * OR_LATENT;
+            oracle_attend(qh, keys, nk, jb->softmax_scale, jb->sink != NULL, jb->sink ? (double)jb->sink[h] : 0.0, o,
+                          jb->lse + (int64_t)w * jb->num_heads + h);
+        }
+    }
+    free(list);
+    free(keys);
+    return NULL;
+}
+
+/* Full decode for a subset of tokens (tokens == NULL: all, in order).  out is
+ * fp64 [n_todo, H, 512] and lse fp64 [n_todo, H], rows in the order of
+ * `tokens`.  Keys whose block-table lookup is out of range are skipped and
+ * counted; the count is returned. */
+int64_t oracle_sparse_mla_decode(const uint16_t *q, int64_t q_token_stride, const uint8_t *kv_cache,
+                                 int32_t num_blocks, int32_t page_block, const int32_t *block_table,
+                                 int64_t bt_stride, int32_t max_blocks, int32_t num_reqs, const int32_t *req_idx,
+                                 const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width,
+                                 const int32_t *topk_lens, const int32_t *seq_lens, int32_t num_tokens,
+                                 int32_t num_heads, int32_t window, const float *sink, double softmax_scale,
+                                 double *out, double *lse, const int32_t *tokens, int32_t n_tokens_todo,
+                                 int32_t n_threads)
+{
+    if (n_threads < 1)
+        n_threads = 1;
+    if (tokens == NULL)
+        n_tokens_todo = num_tokens;
+    if (n_threads > n_tokens_todo)
+        n_threads = n_tokens_todo > 0 ? n_tokens_todo : 1;
+    decode_job *jobs = (decode_job *)calloc((size_t)n_threads, sizeof(decode_job));
+    pthread_t *th = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));
+    for (int32_t i = 0; i < n_threads; ++i) {
+        decode_job *jb = &jobs[i];
+        jb->q = q;
+        jb->q_token_stride = q_token_stride;
+        jb->kv_cache = kv_cache;
+        jb->num_blocks = num_blocks;
+        jb->page_block = page_block;
+        jb->block_table = block_table;
+        jb->bt_stride = bt_stride;
+        jb->max_blocks = max_blocks;
+        jb->num_reqs = num_reqs;
+        jb->req_idx = req_idx;
+        jb->topk_idx = topk_idx;
+        jb->topk_stride = topk_stride;
+        jb->topk_width = topk_width;
+        jb->topk_lens = topk_lens;
+        jb->seq_lens = seq_lens;
+        jb->num_tokens = num_tokens;
+        jb->num_heads = num_heads;
+        jb->window = window;
+        jb->sink = sink;
+        jb->softmax_scale = softmax_scale;
+        jb->out = out;
+        jb->lse = lse;
+        jb->tokens = tokens;
+        jb->n_tokens_todo = n_tokens_todo;
+        jb->worker = i;
+        jb->n_workers = n_threads;
+    }
+    for (int32_t i = 1; i < n_threads; ++i)
+        pthread_create(&th[i], NULL, decode_worker, &jobs[i]);
+    decode_worker(&jobs[0]);
+    int64_t bad = jobs[0].bad;
+    for (int32_t i = 1; i < n_threads; ++i) {
+        pthread_join(th[i], NULL);
+        bad += jobs[i].bad;
+    }
+    free(jobs);
+    free(th);
+    return bad;
+}

@@ -1,0 +1,62 @@
+"""Plants plausible mistakes in copies of the oracle (CPU only) and checks that
+the pins of tests/oracle_pins.py catch every one of them.
+
+Each mutant is oracle.c with one textual change, compiled into a temporary
+library; the real oracle.c is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+# (name, original text, replacement) -- each original must occur in oracle.c; a tuple
+# pair applies several replacements to one mutant
+MUTANTS = [
+    ("rope dropped from the logit", "for (int d = 0; d < OR_DIM; ++d)\n            acc +=",
+     "for (int d = 0; d < OR_LATENT; ++d)\n            acc +="),
+    ("value read from the wrong dims", "out[d] += w * keys[(int64_t)j * OR_DIM + d];",
+     "out[d] += w * keys[(int64_t)j * OR_DIM + d + 64];"),
+    ("sink scaled like a logit", "jb->sink ? (double)jb->sink[h] : 0.0", "jb->sink ? (double)jb->sink[h] * jb->softmax_scale : 0.0"),
+    ("sink left out of the normaliser", "    if (has_sink)\n        z += exp(sink - m);\n    double l = m + log(z);\n    for (int32_t j",
+     "    double l = m + log(z);\n    for (int32_t j"),
+    ("window one too long", "int32_t win_lo = pos - window + 1;", "int32_t win_lo = pos - window;"),
+    ("window not excluded from top-k", "if (v >= win_lo)\n            continue;", "if (v > pos + 1)\n            continue;"),
+    ("no dedup of repeats", "if (row[j] == v) {", "if (0) {"),
+    ("non-causal entries kept", ("if (v < 0 || v > pos)", "if (v >= win_lo)\n            continue;"),
+     ("if (v < 0)", "if (v >= win_lo && v <= pos)\n            continue;")),
+    ("position = seq_len", "int32_t pos = seq_len - 1;", "int32_t pos = seq_len;"),
+    ("scale bias off by one", "return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 128);"),
+    ("scale block of 64", "entry[OR_SCALE_OFF + d / OR_SCALE_BLOCK]", "entry[OR_SCALE_OFF + (d / 64) % 4]"),
+    ("e4m3 bias 8", "v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("e4m3 subnormal scale", "v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
+    ("rope byte order", "(uint16_t)entry[OR_ROPE_OFF + 2 * i] | (uint16_t)((uint16_t)entry[OR_ROPE_OFF + 2 * i + 1] << 8)",
+     "(uint16_t)entry[OR_ROPE_OFF + 2 * i + 1] | (uint16_t)((uint16_t)entry[OR_ROPE_OFF + 2 * i] << 8)"),
+    ("in-page offset shifted", "int32_t off = idx % jb->page_block;", "int32_t off = (idx + 1) % jb->page_block;"),
+    ("request row ignored", "int32_t row = jb->req_idx ? jb->req_idx[t] : t;", "int32_t row = t;"),
+    ("topk_lens ignored", "int32_t n = jb->topk_lens ? jb->topk_lens[t] : jb->topk_width;", "int32_t n = jb->topk_width;"),
+    ("merge weights against the max", "double w = exp(lse_parts[c] - l);", "double w = exp(lse_parts[c] - m);"),
+    ("lse without the log", "double l = m + log(z);\n    for (int32_t j", "double l = m + z;\n    for (int32_t j"),
+    ("softmax scale dropped", "s[j] = softmax_scale * acc;", "s[j] = acc;"),
+]
+
+
+@pytest.mark.parametrize("name,orig,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, orig, repl, tmp_path):
+    mutated = open(oracle.SOURCE).read()
+    origs, repls = (orig, repl) if isinstance(orig, tuple) else ((orig,), (repl,))
+    for o, r in zip(origs, repls):
+        assert mutated.count(o) >= 1, f"mutation site not found: {name}"
+        mutated = mutated.replace(o, r, 1)
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    lib = oracle.compile_source(str(path), str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except (AssertionError, ValueError):
+            caught.append(check.__name__)
+    assert caught, f"no pin caught the mutant '{name}'"
