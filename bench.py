@@ -1,0 +1,522 @@
+#!/usr/bin/env python
+"""Benchmark of one DeepSeek-V4 sparse-MLA decode step on GB300.
+
+A step is one call of dsv4_sparse_mla_decode (index combine + gather/dequant +
+attention + split merge) over the mid-size decode workload: 32 query tokens,
+64 heads, 8192-token histories in 64-token pages, top-k 512, window 128, FP8
+E4M3 + UE8M0 latent and BF16 rope in the cache, BF16 queries.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+ours: inputs resident in HBM; K steps replayed from CUDA graphs, each step on
+one of R replicas of the whole workload (cache pages, block tables, queries,
+outputs) so the bytes the timed steps gather exceed 4x the L2; CUDA events on
+the launching stream, barrier + synchronize on both sides, max over ranks.
+Per-kernel durations for the roofline come from CUPTI kernel records (torch
+profiler) over one extra replay.  e2e repeats the step through the same C ABI
+from pinned host buffers with the host<->device copies inside the timed region.
+N > 1: every rank decodes its own batch on its own GPU (no data-path
+collective; weak scaling).
+
+reference: the fp64 CPU oracle on the host cores, K + W steps of a bounded
+sample (some tokens x some heads) of the same workload, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA decode query-tokens/s; gathered-KV GB/s & TFLOP/s as % of roofline"
+UNIT = "tokens/s"
+WORKLOAD = 2
+KV_BYTES_PER_KEY = 644          # 512 E4M3 + 64 x BF16 + 4 UE8M0 (padding not counted)
+FLOPS_PER_KEY_HEAD = 2 * (576 + 512)
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=WORKLOAD, help="decode workload 1..5 (default: 2, mid decode)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "tokens_per_step": w.num_tokens, "heads": w.num_heads,
+           "seq_len": int(w.seq_lens.max()), "topk": w.topk_width, "window": w.window, "page_block": w.page,
+           "kv_entry": "512 x E4M3 + 4 x UE8M0 (per 128) latent, 64 x BF16 rope, 656 B",
+           "sink": w.sink is not None}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def combined_lengths(w):
+    """Per-token number of keys (distinct valid top-k outside the window + window length)."""
+    lens = np.zeros(w.num_tokens, dtype=np.int64)
+    for t in range(w.num_tokens):
+        pos = int(w.seq_lens[t]) - 1
+        n = w.topk_width if w.topk_lens is None else int(min(max(w.topk_lens[t], 0), w.topk_width))
+        lo = max(0, pos - w.window + 1)
+        v = w.topk_idx[t, :n]
+        lens[t] = np.unique(v[(v >= 0) & (v < lo)]).size + (pos - lo + 1 if pos >= 0 else 0)
+    return lens
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid.lower()
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            self.samples.append((time.time(), parts[0].lower(), parts[1:]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        uids = {u for (_, u, _) in self.samples}
+        mine = {u for u in uids if self.uuid and (self.uuid in u or u in self.uuid)}
+        if not mine and len(uids) == 1:
+            mine = uids
+        samples = [(ts, s) for (ts, u, s) in self.samples if u in mine]
+        inside = [s for (ts, s) in samples if t0 <= ts <= t1]
+        if not inside and samples:   # timed region shorter than the sampling period: nearest sample
+            mid = 0.5 * (t0 + t1)
+            inside = [min(samples, key=lambda x: abs(x[0] - mid))[1]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(s[0]) for s in inside]
+        mx = [num(s[1]) for s in inside]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if s[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": reasons, "samples": len(inside),
+                "power_w_max": max(num(s[2]) for s in inside)}
+
+
+# ----------------------------------------------------------------------------
+# oracle CPU baseline / reference arm
+# ----------------------------------------------------------------------------
+def cpu_baseline(w, seconds: float):
+    import oracle
+    cores = os.cpu_count() or 1
+    oracle.sparse_mla_decode(w, tokens=[0], n_threads=1)     # load + warm
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.sparse_mla_decode(w, n_threads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": reps * w.num_tokens / el, "unit": UNIT, "cores": min(cores, w.num_tokens), "kind": "oracle",
+            "sample": f"all {w.num_tokens} tokens x {w.num_heads} heads of the workload, repeated {reps}x "
+                      f"({el:.1f} s, fp64, one thread per token)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    import synth
+    w = synth.config(args.workload)
+    cores = os.cpu_count() or 1
+    H, T = w.num_heads, w.num_tokens
+    ntok = min(T, cores)
+    # size one step so that warmup + steps end within ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    oracle.sparse_mla_decode(w, tokens=list(range(ntok)), n_threads=ntok, heads=(0, 1))
+    t0 = time.perf_counter()
+    oracle.sparse_mla_decode(w, tokens=list(range(ntok)), n_threads=ntok, heads=(0, 1))
+    t1 = time.perf_counter() - t0
+    hs = 1
+    while hs * 2 <= H and t1 * hs * 2 <= budget:
+        hs *= 2
+    while ntok > 1 and t1 * hs > budget:
+        ntok //= 2
+    toks = [list(range(ntok))]
+
+    def step(i):
+        h0 = (i * hs) % H
+        sel = [(i * ntok + j) % T for j in range(ntok)]
+        oracle.sparse_mla_decode(w, tokens=sel, n_threads=ntok, heads=(h0, h0 + hs))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    el = time.perf_counter() - t0
+    tokens = args.steps * ntok * hs / H
+    value = tokens / el
+    sample = f"{ntok} tokens x {hs} of {H} heads per step (fp64 oracle, {ntok} threads)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, {"reference": "CPU fp64 oracle (no GPU)"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": ntok, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    del toks
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def kernel_times_cupti(replay, names_of_interest=("decode", "combine", "merge")):
+    """Average device duration (us) and count of each of our kernels over one replay()."""
+    import torch
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        replay()
+        torch.cuda.synchronize()
+    stats = {}
+    for ev in prof.events():
+        name = ev.name
+        if not any(k in name for k in names_of_interest):
+            continue
+        dur = getattr(ev, "device_time", None)
+        if dur is None:
+            dur = getattr(ev, "cuda_time", 0.0)
+        s = stats.setdefault(name, [0, 0.0])
+        s[0] += 1
+        s[1] += float(dur)
+    return {k: {"launches": v[0], "avg_us": v[1] / max(1, v[0])} for k, v in stats.items()}
+
+
+def traffic_record(kernel_key: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            recs = json.load(f)
+    except Exception:
+        return None
+    for r in recs:
+        if r.get("kernel") != kernel_key or r.get("workload") != workload:
+            continue
+        src = os.path.join(ROOT, r["source"])
+        try:
+            h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        except OSError:
+            return None
+        return r["dram_bytes_per_launch"] if h == r.get("source_sha256") else None
+    return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    import sparse_mla_decode_combine_gb300 as pkg
+    from sparse_mla_decode_combine_gb300 import build as pkg_build
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or world == 1:
+        pkg_build.build()
+    if world > 1:
+        dist.barrier()
+    pkg.load_library()
+
+    w = synth.config(args.workload)
+    base = synth.to_device(w, dev)
+    T, H, K, W = w.num_tokens, w.num_heads, w.topk_width, w.window
+    lens = combined_lengths(w)
+    keys_per_step = int(lens.sum())
+    bytes_per_step = keys_per_step * KV_BYTES_PER_KEY
+    flops_per_step = keys_per_step * H * FLOPS_PER_KEY_HEAD
+
+    # replicas of the whole workload at distinct addresses: gathered bytes over one rotation >= 4 x L2
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    cache_bytes = base["kv_cache"].numel()
+    R = max(2, math.ceil(4 * l2 / max(1, bytes_per_step)))
+    R = int(min(R, max(2, (24 << 30) // max(1, cache_bytes))))
+    nb = w.num_blocks
+    pool = torch.empty((R * nb, w.page, 656), dtype=torch.uint8, device=dev)
+    bts, qs, outs, lses = [], [], [], []
+    for r in range(R):
+        pool[r * nb:(r + 1) * nb].copy_(base["kv_cache"])
+        bt = base["block_table"]
+        bts.append(torch.where(bt >= 0, bt + r * nb, bt).contiguous())
+        qs.append(base["q"].clone())
+        outs.append(torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev))
+        lses.append(torch.empty((T, H), dtype=torch.float32, device=dev))
+    del base["kv_cache"]
+    ws = pkg.workspace_for(T, H, K, W, dev)
+
+    def step(i):
+        r = i % R
+        return pkg.dsv4_sparse_mla_decode(qs[r], pool, bts[r], base["req_idx"], base["topk_idx"], base["topk_lens"],
+                                          base["seq_lens"], W, base["sink"], base["softmax_scale"], outs[r], lses[r],
+                                          ws)
+
+    # first calls outside capture: library setup, kernel attributes, correctness of the status
+    for i in range(R):
+        pkg.check(step(i), "decode")
+    torch.cuda.synchronize()
+    pkg.check(pkg.dsv4_get_device_status(), "device status")
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def capture(n_steps, start):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_steps):
+                rc = step(start + i)
+                if rc != 0:
+                    raise RuntimeError(f"decode failed during capture: {rc}")
+        return g
+
+    G = R * max(1, math.ceil(64 / R))            # steps per graph: whole rotations
+    g_full = capture(G, 0)
+    nrep, rem = divmod(args.steps, G)
+    g_rem = capture(rem, 0) if rem else None
+    wrep, wrem = divmod(args.warmup, G)
+    g_wrem = capture(wrem, 0) if wrem else None
+
+    with torch.cuda.stream(stream):
+        for _ in range(wrep):
+            g_full.replay()
+        if g_wrem is not None:
+            g_wrem.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.5)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    h0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(nrep):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if rank == 0:
+        time.sleep(0.2)
+        sampler.stop()
+    clocks = sampler.summary(h0, h1) if rank == 0 else None
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    value = world * T * args.steps / (ms / 1e3)
+
+    # per-kernel device durations (CUPTI) over one rotation of direct calls (the same launches the
+    # graphs hold), for the roofline and the launch count
+    def one_rotation():
+        with torch.cuda.stream(stream):
+            for i in range(G):
+                step(i)
+    try:
+        kt = kernel_times_cupti(one_rotation)
+    except Exception as e:  # profiler unavailable: no roofline numbers
+        kt = {"error": str(e)}
+    launches_per_step = sum(v["launches"] for v in kt.values() if isinstance(v, dict)) / G if "error" not in kt else None
+    decode_name = None
+    if "error" not in kt:
+        dec = {k: v for k, v in kt.items() if "decode" in k}
+        if dec:
+            decode_name = max(dec, key=lambda k: dec[k]["avg_us"] * dec[k]["launches"])
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+    roofline = None
+    if decode_name is not None:
+        dur_s = kt[decode_name]["avg_us"] * 1e-6
+        achieved = bytes_per_step / dur_s / 1e9
+        t_hbm = bytes_per_step / (hbm_peak * 1e9)
+        t_tc = flops_per_step / (bf16_peak * 1e12)
+        bound = "hbm" if t_hbm >= t_tc else "tensor"
+        if bound == "hbm":
+            roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": achieved / hbm_peak}
+        else:
+            ach_t = flops_per_step / dur_s / 1e12
+            roofline = {"bound": "tensor", "achieved": ach_t, "peak": bf16_peak, "unit": "TFLOP/s",
+                        "frac": ach_t / bf16_peak}
+        m = re.search(r"(\w+_kernel)", decode_name)
+        roofline.update({"traffic": traffic_record(m.group(1) if m else decode_name, w.name),
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+                         "kernel": decode_name, "kernel_avg_us": kt[decode_name]["avg_us"],
+                         "kernel_time_method": "CUPTI kernel records (torch.profiler) over one graph replay of "
+                                               f"{G} steps",
+                         "algorithmic_bytes_per_launch": bytes_per_step, "flops_per_launch": flops_per_step,
+                         "step_roofline_frac": max(t_hbm, t_tc) / (ms / 1e3 / args.steps),
+                         "kv_gbs_step": bytes_per_step * args.steps / (ms / 1e3) / 1e9,
+                         "tflops_step": flops_per_step * args.steps / (ms / 1e3) / 1e12})
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq = w.q.view(np.int16)
+        host = {"q": torch.from_numpy(np.ascontiguousarray(hq)).view(torch.bfloat16).pin_memory(),
+                "block_table": torch.from_numpy(w.block_table).pin_memory(),
+                "topk_idx": torch.from_numpy(w.topk_idx).pin_memory(),
+                "seq_lens": torch.from_numpy(w.seq_lens).pin_memory()}
+        if w.topk_lens is not None:
+            host["topk_lens"] = torch.from_numpy(w.topk_lens).pin_memory()
+        if w.req_idx is not None:
+            host["req_idx"] = torch.from_numpy(w.req_idx).pin_memory()
+        devbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        h_out = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
+        h_lse = torch.empty((T, H), dtype=torch.float32).pin_memory()
+        d_out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+        d_lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        pool0 = pool[:nb]
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = h_out.numel() * 2 + h_lse.numel() * 4
+        n_e2e = args.steps
+
+        def e2e_step():
+            for k, v in host.items():
+                devbuf[k].copy_(v, non_blocking=True)
+            rc = pkg.dsv4_sparse_mla_decode(devbuf["q"], pool0, devbuf["block_table"], devbuf.get("req_idx"),
+                                            devbuf["topk_idx"], devbuf.get("topk_lens"), devbuf["seq_lens"], W,
+                                            base["sink"], base["softmax_scale"], d_out, d_lse, ws)
+            h_out.copy_(d_out, non_blocking=True)
+            h_lse.copy_(d_lse, non_blocking=True)
+            return rc
+
+        with torch.cuda.stream(stream):
+            for _ in range(min(args.warmup, 50)):
+                e2e_step()
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * T * n_e2e / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "method": "per step: pinned H2D of q/topk/seq_lens/block_table, the C-ABI call, D2H of out+lse"}
+
+    pkg.check(pkg.dsv4_get_device_status(), "device status")
+
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(w, args.cpu_seconds)
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic",
+                "config": workload_config(w, {"l2": f"inputs larger than L2: {R} rotating replicas "
+                                                    f"({R * bytes_per_step / 1e6:.0f} MB gathered per rotation, "
+                                                    f"L2 {l2 / 1e6:.0f} MB)",
+                                              "replicas": R, "keys_per_step": keys_per_step}),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": None if launches_per_step is None else int(round(launches_per_step * args.steps)),
+                "kernels": kt, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,190 @@
+/*
+ * dsv4.h -- C ABI of the GB300 (sm_103a) DeepSeek-V4 sparse-MLA decode library.
+ *
+ * One decode step for a batch of query tokens over a paged FP8 KV cache:
+ *   1. per token, merge the top-k selected positions with the sliding window
+ *      (SWA), dropping invalid, non-causal, in-window and repeated entries;
+ *   2. translate each logical position to a physical cache slot through the
+ *      block table and gather + dequantise the 656-byte entries;
+ *   3. MQA attention of all heads over those keys: logits over the 576-d key
+ *      (512 latent + 64 RoPE), values = the 512-d latent, an optional per-head
+ *      sink logit in the softmax normaliser;
+ *   4. BF16 output [T, H, 512] and a natural-log LSE per (token, head).
+ *
+ * Sources of the operations (vLLM pull-request summaries):
+ *   - "[ROCm] [DSv4] [Perf] Support DeepSeek v4 MTP" (vllm #43385), section
+ *     "关键源码片段 / rocm.py": _combine_topk_swa_indices_kernel / combine_topk_swa_indices
+ *     (top-k entries then the window [pos - swa_len + 1, pos], swa_len = min(pos + 1, W),
+ *     validity test, combined_lens = topk part + swa part, 128-aligned padded width).
+ *   - "feat: add DeepSeek-V4 XPU attention decode path" (vllm #42953), section
+ *     "xpu_sparse_decode_fp8.py": _dequant_gather_slots_kernel (slot -> block / offset,
+ *     value = e4m3 * exp2(ue8m0 - 127), negative slot -> no contribution) and
+ *     xpu_sparse_decode_fp8 / triton_bf16_mla_sparse_interface (sparse MLA over the
+ *     gathered keys, with per-token top-k lengths).
+ *   - "Enable DeepSeek V4 and GLM-5.1 on SM120" (vllm #43477), section
+ *     "flashinfer_mla_sparse_sm120.py": forward_mqa converts per-request top-k indices to
+ *     physical slots through the block table and writes output [T, h, kv_lora_rank = 512];
+ *     "flashinfer_sparse.py": supports_sink.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *     all memory.  The library never allocates device memory in a call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and never synchronise it.  Kernels run on the current CUDA device.
+ *   - Argument errors are detected on the host and returned before anything is
+ *     enqueued.  Errors that depend on device data (an out-of-range block-table entry,
+ *     an out-of-range request index) do not stop the kernels: the offending key is left
+ *     out of the result and a sticky per-device status word records the error; read it
+ *     with dsv4_get_device_status().
+ *   - All integer sizes and strides are in elements of the array's own type.
+ *
+ * KV-cache entry (656 bytes; entries are token-major inside a page, page stride
+ * page_block * 656 bytes):
+ *   [0, 512)    512 E4M3FN latent codes (OCP FP8: bias 7, max 448, S.1111.111 = NaN)
+ *   [512, 640)  64 BF16 RoPE values, little-endian
+ *   [640, 644)  4 UE8M0 scale bytes; byte b scales latent dims [128 b, 128 b + 128) by 2^(byte - 127)
+ *   [644, 656)  padding (not read as data)
+ * The key is k = [latent * scale, rope] (576 dims); the value is v = latent * scale (512 dims).
+ */
+#ifndef DSV4_H_
+#define DSV4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DSV4_API __attribute__((visibility("default")))
+#else
+#define DSV4_API
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *dsv4_stream_t;
+
+typedef enum dsv4_status {
+    DSV4_OK = 0,
+    DSV4_ERR_INVALID_ARG = 1,   /* bad pointer, size, stride, alignment or workspace size */
+    DSV4_ERR_BAD_INDEX = 2,     /* device status only: a block-table or request index was out of range */
+    DSV4_ERR_TIMEOUT = 3,       /* device status only: a bounded wait inside a kernel gave up */
+    DSV4_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    DSV4_ERR_UNSUPPORTED = 5    /* valid request this build does not implement (e.g. num_heads) */
+} dsv4_status;
+
+/*
+ * dsv4_combine_topk_swa_indices -- per-token index list: kept top-k entries, then the window.
+ *
+ * Source: vllm #43385 "[ROCm] [DSv4] [Perf] Support DeepSeek v4 MTP", section
+ * "关键源码片段 / rocm.py", _combine_topk_swa_indices_kernel.  This library reads one
+ * cache region for both parts, so (where the page's kernel indexes two disjoint regions)
+ * it additionally drops top-k entries that the window already covers and repeats, and
+ * compacts the kept entries.
+ *
+ * For token t with pos = seq_lens[t] - 1 and n = min(max(topk_lens[t], 0), topk_width)
+ * (n = topk_width when topk_lens is NULL):
+ *   window   = [max(0, pos - window + 1), pos]   (empty when pos < 0 or window == 0)
+ *   kept     = topk_idx[t][i] for i < n, in order of i, when 0 <= value <= pos, value is
+ *              not inside the window, and no earlier i' < i holds the same value
+ *   combined[t][0 .. L)      = kept entries, then the window positions ascending
+ *   combined[t][L .. width)  = -1
+ *   combined_lens[t]         = L = |kept| + window length
+ *
+ * Arguments:
+ *   topk_idx        int32 [num_tokens, topk_width], row stride topk_stride (>= topk_width);
+ *                   may be NULL when topk_width == 0.
+ *   topk_width      0 .. 8192.
+ *   topk_lens       int32 [num_tokens] or NULL.
+ *   seq_lens        int32 [num_tokens]: causal visible length of each token (its position + 1).
+ *   num_tokens      >= 0 (0 enqueues nothing).
+ *   window          >= 0.
+ *   combined        int32 [num_tokens, combined_width], row stride combined_stride (>= combined_width).
+ *   combined_width  >= topk_width + window (callers usually round up to a multiple of 128).
+ *   combined_lens   int32 [num_tokens].
+ * Returns DSV4_OK, DSV4_ERR_INVALID_ARG, DSV4_ERR_UNSUPPORTED (topk_width > 8192) or DSV4_ERR_CUDA.
+ */
+DSV4_API dsv4_status dsv4_combine_topk_swa_indices(const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width,
+                                          const int32_t *topk_lens, const int32_t *seq_lens, int32_t num_tokens,
+                                          int32_t window, int32_t *combined, int64_t combined_stride,
+                                          int32_t combined_width, int32_t *combined_lens, dsv4_stream_t stream);
+
+/*
+ * dsv4_sparse_mla_decode_workspace_size -- bytes of device workspace dsv4_sparse_mla_decode needs.
+ *
+ * The size depends on the arguments and on the multiprocessor count of the current
+ * CUDA device (it fixes how many workers share one token's keys); query it with the
+ * device that will run the decode current.  Returns 0 for arguments the decode rejects.
+ */
+DSV4_API size_t dsv4_sparse_mla_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk_width,
+                                             int32_t window);
+
+/*
+ * dsv4_sparse_mla_decode -- one sparse-MLA decode step (combine + gather/dequant + attention).
+ *
+ * Sources: the three pages named at the top of this file (combine: vllm #43385 rocm.py;
+ * gather + dequant + BF16 sparse MLA: vllm #42953 xpu_sparse_decode_fp8.py; block-table
+ * conversion, output [T, h, 512], sinks: vllm #43477 flashinfer_mla_sparse_sm120.py).
+ *
+ * For each token t and head h, with K_t the token's combined index list (as
+ * dsv4_combine_topk_swa_indices with this call's arguments), row r = req_idx[t] (t when
+ * req_idx is NULL), and for each logical position p in K_t the cache entry at
+ *     slot = block_table[r][p / page_block] * page_block + p % page_block:
+ *   s_p        = softmax_scale * sum_{d < 576} q[t][h][d] * k_p[d]
+ *   lse[t][h]  = ln( sum_p e^{s_p} + e^{sink[h]} )        (no sink term when sink is NULL)
+ *   out[t][h]  = sum_p e^{s_p - lse[t][h]} * v_p            (BF16, round-to-nearest-even)
+ * A token with no key and no sink gets out = 0 and lse = -inf.  The sink is a logit in
+ * the same units as s (it is not multiplied by softmax_scale).
+ *
+ * Arguments:
+ *   q               BF16 [num_tokens, num_heads, 576]; heads contiguous (stride 576),
+ *                   tokens at stride q_token_stride (>= num_heads * 576, multiple of 8).
+ *                   16-byte aligned.
+ *   kv_cache        uint8 [num_blocks, page_block, 656] (layout above), 16-byte aligned.
+ *   block_table     int32 [num_reqs, max_blocks], row stride bt_stride (>= max_blocks).
+ *                   Entries read must lie in [0, num_blocks); others are data errors.
+ *   req_idx         int32 [num_tokens]: the block-table row of each token, in [0, num_reqs);
+ *                   NULL means row t (then num_reqs >= num_tokens).  Several tokens may
+ *                   share a row (speculative verify: one request, several positions).
+ *   topk_idx, topk_stride, topk_width, topk_lens, seq_lens, window: as in
+ *                   dsv4_combine_topk_swa_indices.  seq_lens[t] - 1 must be < max_blocks *
+ *                   page_block for positions the token reads; others are data errors.
+ *   num_tokens      >= 0 (0 enqueues nothing).
+ *   num_heads       16, 32, 64 or 128 (others: DSV4_ERR_UNSUPPORTED).
+ *   sink            float32 [num_heads] or NULL.
+ *   softmax_scale   finite.
+ *   out             BF16 [num_tokens, num_heads, 512], contiguous, 16-byte aligned.
+ *   lse             float32 [num_tokens, num_heads], contiguous, or NULL.
+ *   workspace       device scratch of at least dsv4_sparse_mla_decode_workspace_size(...)
+ *                   bytes, 256-byte aligned, not used by anything else until the work
+ *                   enqueued by this call has finished.  Its contents on entry do not matter.
+ *   stream          CUDA stream.
+ * Returns DSV4_OK, DSV4_ERR_INVALID_ARG, DSV4_ERR_UNSUPPORTED or DSV4_ERR_CUDA.
+ */
+DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_token_stride, const void *kv_cache, int32_t num_blocks,
+                                   int32_t page_block, const int32_t *block_table, int64_t bt_stride,
+                                   int32_t max_blocks, int32_t num_reqs, const int32_t *req_idx,
+                                   const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width,
+                                   const int32_t *topk_lens, const int32_t *seq_lens, int32_t num_tokens,
+                                   int32_t num_heads, int32_t window, const float *sink, float softmax_scale,
+                                   void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                   dsv4_stream_t stream);
+
+/*
+ * dsv4_get_device_status -- synchronise `stream`, then read and clear the current
+ * device's sticky status word.
+ *
+ * Returns DSV4_OK when no kernel of this library on the current device recorded a data
+ * error since the last call, DSV4_ERR_BAD_INDEX or DSV4_ERR_TIMEOUT for the recorded
+ * error (BAD_INDEX wins when both were recorded), or DSV4_ERR_CUDA when the
+ * synchronisation or the read failed.  The word is shared by all streams of the device.
+ */
+DSV4_API dsv4_status dsv4_get_device_status(dsv4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSV4_H_ */

@@ -77,7 +77,7 @@ class Oracle:
         lib.oracle_merge.argtypes = [i32, P, P, ctypes.c_int, f64, P, P]
         lib.oracle_sparse_mla_decode.restype = i64
         lib.oracle_sparse_mla_decode.argtypes = [P, i64, P, i32, i32, P, i64, i32, i32, P, P, i64, i32, P, P,
-                                                 i32, i32, i32, P, f64, P, P, P, i32, i32]
+                                                 i32, i32, i32, P, f64, P, P, P, i32, i32, i32, i32]
         self.lib = lib
 
     def e4m3_to_f64(self, code: int) -> float:
@@ -128,11 +128,13 @@ class Oracle:
                               0.0 if sink is None else float(sink), _ptr(out), _ptr(lse))
         return out, float(lse[0])
 
-    def sparse_mla_decode(self, w, tokens: Optional[Sequence[int]] = None, n_threads: Optional[int] = None):
+    def sparse_mla_decode(self, w, tokens: Optional[Sequence[int]] = None, n_threads: Optional[int] = None,
+                          heads: Optional[tuple] = None):
         """Decode for workload `w` (a synth.Workload or anything with the same fields).
 
-        Returns (out fp64 [n, H, 512], lse fp64 [n, H], bad_key_count); rows follow
-        `tokens` (default: all tokens in order).
+        Returns (out fp64 [n, nh, 512], lse fp64 [n, nh], bad_key_count); rows follow
+        `tokens` (default: all tokens in order), heads the range `heads` = (begin, end)
+        (default: all heads).
         """
         q = _c(w.q, np.uint16)
         T, H, D = q.shape
@@ -143,15 +145,18 @@ class Oracle:
         tk = _c(w.topk_idx, np.int32)
         tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
         n = T if tok is None else tok.size
-        out = np.zeros((n, H, 512), dtype=np.float64)
-        lse = np.zeros((n, H), dtype=np.float64)
+        h0, h1 = (0, H) if heads is None else (int(heads[0]), int(heads[1]))
+        assert 0 <= h0 <= h1 <= H
+        out = np.zeros((n, h1 - h0, 512), dtype=np.float64)
+        lse = np.zeros((n, h1 - h0), dtype=np.float64)
         if n_threads is None:
             n_threads = os.cpu_count() or 1
         bad = self.lib.oracle_sparse_mla_decode(
             _ptr(q), H * 576, _ptr(cache), cache.shape[0], cache.shape[1], _ptr(bt), bt.shape[1], bt.shape[1],
             bt.shape[0], _ptr(_c(w.req_idx, np.int32)), _ptr(tk), tk.shape[1], tk.shape[1],
             _ptr(_c(w.topk_lens, np.int32)), _ptr(_c(w.seq_lens, np.int32)), T, H, int(w.window),
-            _ptr(_c(w.sink, np.float32)), float(w.softmax_scale), _ptr(out), _ptr(lse), _ptr(tok), n, int(n_threads))
+            _ptr(_c(w.sink, np.float32)), float(w.softmax_scale), _ptr(out), _ptr(lse), _ptr(tok), n, h0, h1,
+            int(n_threads))
         return out, lse, int(bad)
 
 
@@ -191,5 +196,5 @@ def merge(lse_parts, out_parts, sink=None):
     return default().merge(lse_parts, out_parts, sink)
 
 
-def sparse_mla_decode(w, tokens=None, n_threads=None):
-    return default().sparse_mla_decode(w, tokens, n_threads)
+def sparse_mla_decode(w, tokens=None, n_threads=None, heads=None):
+    return default().sparse_mla_decode(w, tokens, n_threads, heads)

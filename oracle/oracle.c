@@ -249,6 +249,7 @@ typedef struct {
     int32_t topk_width;
     const int32_t *topk_lens, *seq_lens;
     int32_t num_tokens, num_heads, window;
+    int32_t head_begin, head_end;
     const float *sink;
     double softmax_scale;
     double *out, *lse;
@@ -294,13 +295,15 @@ static void *decode_worker(void *arg)
             oracle_dequant_entry(jb->kv_cache + slot * OR_ENTRY_BYTES, keys + (int64_t)nk * OR_DIM);
             nk++;
         }
-        for (int32_t h = 0; h < jb->num_heads; ++h) {
+        int32_t nh = jb->head_end - jb->head_begin;
+        for (int32_t h = jb->head_begin; h < jb->head_end; ++h) {
             const uint16_t *qp = jb->q + (int64_t)t * jb->q_token_stride + (int64_t)h * OR_DIM;
             for (int d = 0; d < OR_DIM; ++d)
                 qh[d] = oracle_bf16_to_double(qp[d]);
-            double *o = jb->out + ((int64_t)w * jb->num_heads + h) * OR_LATENT;
+            int64_t r = (int64_t)w * nh + (h - jb->head_begin);
+            double *o = jb->out + r * OR_LATENT;
             oracle_attend(qh, keys, nk, jb->softmax_scale, jb->sink != NULL, jb->sink ? (double)jb->sink[h] : 0.0, o,
-                          jb->lse + (int64_t)w * jb->num_heads + h);
+                          jb->lse + r);
         }
     }
     free(list);
@@ -308,10 +311,11 @@ static void *decode_worker(void *arg)
     return NULL;
 }
 
-/* Full decode for a subset of tokens (tokens == NULL: all, in order).  out is
- * fp64 [n_todo, H, 512] and lse fp64 [n_todo, H], rows in the order of
- * `tokens`.  Keys whose block-table lookup is out of range are skipped and
- * counted; the count is returned. */
+/* Full decode for a subset of tokens (tokens == NULL: all, in order) and the heads
+ * [head_begin, head_end).  out is fp64 [n_todo, head_end - head_begin, 512] and
+ * lse fp64 [n_todo, head_end - head_begin], rows in the order of `tokens`.  Keys
+ * whose block-table lookup is out of range are skipped and counted; the count is
+ * returned. */
 int64_t oracle_sparse_mla_decode(const uint16_t *q, int64_t q_token_stride, const uint8_t *kv_cache,
                                  int32_t num_blocks, int32_t page_block, const int32_t *block_table,
                                  int64_t bt_stride, int32_t max_blocks, int32_t num_reqs, const int32_t *req_idx,
@@ -319,7 +323,7 @@ int64_t oracle_sparse_mla_decode(const uint16_t *q, int64_t q_token_stride, cons
                                  const int32_t *topk_lens, const int32_t *seq_lens, int32_t num_tokens,
                                  int32_t num_heads, int32_t window, const float *sink, double softmax_scale,
                                  double *out, double *lse, const int32_t *tokens, int32_t n_tokens_todo,
-                                 int32_t n_threads)
+                                 int32_t head_begin, int32_t head_end, int32_t n_threads)
 {
     if (n_threads < 1)
         n_threads = 1;
@@ -349,6 +353,8 @@ int64_t oracle_sparse_mla_decode(const uint16_t *q, int64_t q_token_stride, cons
         jb->num_tokens = num_tokens;
         jb->num_heads = num_heads;
         jb->window = window;
+        jb->head_begin = head_begin;
+        jb->head_end = head_end;
         jb->sink = sink;
         jb->softmax_scale = softmax_scale;
         jb->out = out;

@@ -1,0 +1,272 @@
+// api.cu -- the C ABI declared in include/dsv4.h: argument validation, the work plan,
+// and the launches on the caller's stream.  No device memory is allocated here; all
+// scratch lives in the caller's workspace.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/dsv4.h"
+#include "internal.h"
+
+namespace dsv4 {
+namespace {
+
+// Sticky per-device status word (bits kStatusBadIndex / kStatusTimeout).
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_status_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+
+// Device address of the status word and the SM count of the current device.
+cudaError_t device_info(unsigned **status, int *sms)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_status_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_status_word);
+        if (e != cudaSuccess)
+            return e;
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        g_sm_count[dev] = n;
+        g_status_ptr[dev] = static_cast<unsigned *>(ptr);
+    }
+    if (status)
+        *status = g_status_ptr[dev];
+    if (sms)
+        *sms = g_sm_count[dev];
+    return cudaSuccess;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kMaxWindow = 1 << 24;
+constexpr int kSimtTile = 32;
+
+bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sms, Plan *pl)
+{
+    if (num_tokens < 0 || topk_width < 0 || topk_width > kMaxTopkWidth || window < 0 || window > kMaxWindow)
+        return false;
+    if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128)
+        return false;
+    Plan p{};
+    p.path = kPathSimt;
+    p.heads_per_group = num_heads == 16 ? 16 : 32;
+    p.groups = num_heads / p.heads_per_group;
+    p.cw = topk_width + window;
+    const int tile = kSimtTile;
+    const long long units0 = (long long)(num_tokens > 0 ? num_tokens : 1) * p.groups;
+    const int max_splits = std::max(1, std::min(merge_max_splits(), (p.cw + tile - 1) / tile));
+    int want = (int)std::min<long long>(max_splits, (sms + units0 - 1) / units0);
+    want = std::max(1, want);
+    int chunk = (p.cw + want - 1) / want;
+    chunk = std::max(tile, (chunk + tile - 1) / tile * tile);
+    p.chunk = chunk;
+    p.splits = std::max(1, (p.cw + chunk - 1) / chunk);
+    p.combine_table_bits = combine_table_bits(topk_width);
+
+    size_t off = 0;
+    p.off_combined = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)num_tokens * (size_t)p.cw, 256);
+    p.off_lens = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)num_tokens, 256);
+    p.off_part_o = off;
+    p.off_part_ml = off;
+    if (p.splits > 1) {
+        off = align_up(off + sizeof(float) * (size_t)num_tokens * p.splits * num_heads * kLatent, 256);
+        p.off_part_ml = off;
+        off = align_up(off + sizeof(float) * 2 * (size_t)num_tokens * p.splits * num_heads, 256);
+    }
+    p.total = std::max<size_t>(off, 256);
+    *pl = p;
+    return true;
+}
+
+dsv4_status check_combine_args(const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width,
+                               const int32_t *seq_lens, int32_t num_tokens, int32_t window)
+{
+    if (num_tokens < 0 || topk_width < 0 || window < 0 || window > kMaxWindow)
+        return DSV4_ERR_INVALID_ARG;
+    if (topk_width > kMaxTopkWidth)
+        return DSV4_ERR_UNSUPPORTED;
+    if (num_tokens > 0) {
+        if (seq_lens == nullptr)
+            return DSV4_ERR_INVALID_ARG;
+        if (topk_width > 0 && (topk_idx == nullptr || topk_stride < topk_width))
+            return DSV4_ERR_INVALID_ARG;
+    }
+    return DSV4_OK;
+}
+
+int g_attr_bytes[kMaxDevices][kAttrSlots];
+
+}  // namespace
+
+cudaError_t set_smem_once(const void *kernel, int bytes, AttrSlot slot)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_attr_bytes[dev][slot] >= bytes)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        g_attr_bytes[dev][slot] = bytes;
+    return e;
+}
+
+}  // namespace dsv4
+
+using namespace dsv4;
+
+extern "C" DSV4_API dsv4_status dsv4_combine_topk_swa_indices(const int32_t *topk_idx, int64_t topk_stride,
+                                                     int32_t topk_width, const int32_t *topk_lens,
+                                                     const int32_t *seq_lens, int32_t num_tokens, int32_t window,
+                                                     int32_t *combined, int64_t combined_stride,
+                                                     int32_t combined_width, int32_t *combined_lens,
+                                                     dsv4_stream_t stream)
+{
+    dsv4_status st = check_combine_args(topk_idx, topk_stride, topk_width, seq_lens, num_tokens, window);
+    if (st != DSV4_OK)
+        return st;
+    if ((long long)combined_width < (long long)topk_width + window)
+        return DSV4_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return DSV4_OK;
+    if (combined == nullptr || combined_lens == nullptr || combined_stride < combined_width)
+        return DSV4_ERR_INVALID_ARG;
+    cudaError_t e = launch_combine(topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens, window,
+                                   combined, combined_stride, combined_width, combined_lens,
+                                   combine_table_bits(topk_width), reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+extern "C" DSV4_API size_t dsv4_sparse_mla_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk_width,
+                                                        int32_t window)
+{
+    int sms = 0;
+    if (device_info(nullptr, &sms) != cudaSuccess)
+        return 0;
+    Plan pl;
+    if (!make_plan(num_tokens, num_heads, topk_width, window, sms, &pl))
+        return 0;
+    return pl.total;
+}
+
+extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_token_stride, const void *kv_cache,
+                                              int32_t num_blocks, int32_t page_block, const int32_t *block_table,
+                                              int64_t bt_stride, int32_t max_blocks, int32_t num_reqs,
+                                              const int32_t *req_idx, const int32_t *topk_idx, int64_t topk_stride,
+                                              int32_t topk_width, const int32_t *topk_lens, const int32_t *seq_lens,
+                                              int32_t num_tokens, int32_t num_heads, int32_t window,
+                                              const float *sink, float softmax_scale, void *out, float *lse,
+                                              void *workspace, size_t workspace_bytes, dsv4_stream_t stream)
+{
+    dsv4_status st = check_combine_args(topk_idx, topk_stride, topk_width, seq_lens, num_tokens, window);
+    if (st != DSV4_OK)
+        return st;
+    if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128)
+        return DSV4_ERR_UNSUPPORTED;
+    if (!std::isfinite(softmax_scale))
+        return DSV4_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return DSV4_OK;
+    if (q == nullptr || kv_cache == nullptr || block_table == nullptr || out == nullptr || workspace == nullptr)
+        return DSV4_ERR_INVALID_ARG;
+    if (q_token_stride < (int64_t)num_heads * kDim || q_token_stride % 8 != 0)
+        return DSV4_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || page_block <= 0 || max_blocks <= 0 || num_reqs <= 0 || bt_stride < max_blocks)
+        return DSV4_ERR_INVALID_ARG;
+    if (req_idx == nullptr && num_reqs < num_tokens)
+        return DSV4_ERR_INVALID_ARG;
+    if ((long long)max_blocks * page_block > INT_MAX)
+        return DSV4_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+        return DSV4_ERR_INVALID_ARG;
+
+    unsigned *status = nullptr;
+    int sms = 0;
+    if (device_info(&status, &sms) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    Plan pl;
+    if (!make_plan(num_tokens, num_heads, topk_width, window, sms, &pl))
+        return DSV4_ERR_INVALID_ARG;
+    if (workspace_bytes < pl.total)
+        return DSV4_ERR_INVALID_ARG;
+
+    char *ws = static_cast<char *>(workspace);
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.q_token_stride = q_token_stride;
+    p.kv = static_cast<const uint8_t *>(kv_cache);
+    p.num_blocks = num_blocks;
+    p.page = page_block;
+    p.block_table = block_table;
+    p.bt_stride = bt_stride;
+    p.max_blocks = max_blocks;
+    p.num_reqs = num_reqs;
+    p.req_idx = req_idx;
+    p.combined = reinterpret_cast<int32_t *>(ws + pl.off_combined);
+    p.cw = pl.cw;
+    p.lens = reinterpret_cast<int32_t *>(ws + pl.off_lens);
+    p.num_tokens = num_tokens;
+    p.num_heads = num_heads;
+    p.sink = sink;
+    p.scale = softmax_scale;
+    p.out = static_cast<uint16_t *>(out);
+    p.lse = lse;
+    p.part_o = reinterpret_cast<float *>(ws + pl.off_part_o);
+    p.part_ml = reinterpret_cast<float *>(ws + pl.off_part_ml);
+    p.groups = pl.groups;
+    p.heads_per_group = pl.heads_per_group;
+    p.splits = pl.splits;
+    p.chunk = pl.chunk;
+    p.status = status;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_combine(topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens, window,
+                                   reinterpret_cast<int32_t *>(ws + pl.off_combined), pl.cw, pl.cw,
+                                   reinterpret_cast<int32_t *>(ws + pl.off_lens), pl.combine_table_bits, s);
+    if (e == cudaSuccess)
+        e = launch_decode_simt(p, s);
+    if (e == cudaSuccess)
+        e = launch_merge(p, s);
+    return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+extern "C" DSV4_API dsv4_status dsv4_get_device_status(dsv4_stream_t stream)
+{
+    unsigned *status = nullptr;
+    if (device_info(&status, nullptr) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    if (word & kStatusBadIndex)
+        return DSV4_ERR_BAD_INDEX;
+    if (word & kStatusTimeout)
+        return DSV4_ERR_TIMEOUT;
+    return DSV4_OK;
+}

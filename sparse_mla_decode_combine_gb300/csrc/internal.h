@@ -1,0 +1,89 @@
+// internal.h -- launch interface between the C ABI (api.cu) and the kernel files.
+// Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dsv4 {
+
+// Cache entry layout (656 bytes): 512 E4M3 latent codes, 64 BF16 rope values,
+// 4 UE8M0 scale bytes, 12 bytes of padding.
+constexpr int kEntryBytes = 656;
+constexpr int kLatent = 512;
+constexpr int kRope = 64;
+constexpr int kDim = 576;
+constexpr int kRopeOffset = 512;
+constexpr int kScaleOffset = 640;
+constexpr int kScaleBlock = 128;
+
+// Bits of the sticky device status word.
+constexpr unsigned kStatusBadIndex = 1u;
+constexpr unsigned kStatusTimeout = 2u;
+
+constexpr int kMaxTopkWidth = 8192;
+
+// Which decode kernel runs a call.
+enum DecodePath { kPathSimt = 0, kPathTc = 1 };
+
+// Work decomposition of one decode call; computed on the host from the call's
+// sizes and the device's SM count, identically by the workspace-size query.
+struct Plan {
+    int path;
+    int heads_per_group;   // heads handled by one worker
+    int groups;            // num_heads / heads_per_group
+    int splits;            // workers sharing one (token, head group); > 1 needs the merge
+    int chunk;             // combined-list entries per split
+    int cw;                // row width of the internal combined list (topk_width + window)
+    int combine_table_bits;
+    size_t off_combined, off_lens, off_part_o, off_part_ml, total;
+};
+
+struct DecodeParams {
+    const uint16_t *q;
+    int64_t q_token_stride;
+    const uint8_t *kv;
+    int32_t num_blocks;
+    int32_t page;
+    const int32_t *block_table;
+    int64_t bt_stride;
+    int32_t max_blocks;
+    int32_t num_reqs;
+    const int32_t *req_idx;
+    const int32_t *combined;   // [T, cw]
+    int32_t cw;
+    const int32_t *lens;       // [T]
+    int32_t num_tokens;
+    int32_t num_heads;
+    const float *sink;
+    float scale;
+    uint16_t *out;             // BF16 [T, H, 512]
+    float *lse;                // [T, H] or null
+    float *part_o;             // [T, groups, splits, hpg, 512] when splits > 1
+    float *part_ml;            // [T, groups, splits, hpg, 2]   (running max, running sum)
+    int32_t groups;
+    int32_t heads_per_group;
+    int32_t splits;
+    int32_t chunk;
+    unsigned *status;
+};
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes`, once per
+// (device, kernel slot); later calls with no larger size touch no CUDA state, so a
+// call made after the first one on a device is safe inside stream capture.
+enum AttrSlot { kAttrCombine = 0, kAttrSimt16, kAttrSimt32, kAttrTc, kAttrSlots };
+cudaError_t set_smem_once(const void *kernel, int bytes, AttrSlot slot);
+
+int combine_table_bits(int topk_width);
+size_t combine_smem_bytes(int table_bits, int topk_width);
+cudaError_t launch_combine(const int32_t *topk, int64_t topk_stride, int topk_width, const int32_t *topk_lens,
+                           const int32_t *seq_lens, int num_tokens, int window, int32_t *combined,
+                           int64_t combined_stride, int combined_width, int32_t *combined_lens, int table_bits,
+                           cudaStream_t stream);
+
+cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams &p, cudaStream_t stream);
+int merge_max_splits();
+
+}  // namespace dsv4

@@ -314,3 +314,17 @@ def small_config(n: int) -> Workload:
         return make_workload(name="small-long", seed=seed, heads=64, req_seq_lens=seqs, topk_width=400,
                              window=96, sink=True, latent_dist="t3")
     raise ValueError(n)
+
+
+def to_device(w: Workload, device="cuda") -> dict:
+    """Copy a workload's arrays into torch tensors on `device` (BF16 q, uint8 cache, int32 indices)."""
+    import torch
+
+    def t(a, dtype):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dtype)
+
+    q = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(torch.bfloat16).to(device)
+    return dict(q=q, kv_cache=t(w.kv_cache, torch.uint8), block_table=t(w.block_table, torch.int32),
+                req_idx=t(w.req_idx, torch.int32), topk_idx=t(w.topk_idx, torch.int32),
+                topk_lens=t(w.topk_lens, torch.int32), seq_lens=t(w.seq_lens, torch.int32),
+                window=int(w.window), sink=t(w.sink, torch.float32), softmax_scale=float(w.softmax_scale))

@@ -1,0 +1,167 @@
+"""GPU parity of dsv4_sparse_mla_decode against the fp64 oracle.
+
+Tolerances (gpu_util): BF16 output max |err| <= 2e-2 and rel-L2 <= 1e-2; LSE |err| <= 1e-3.
+Small versions of the five workloads run whole; the full-size workloads run in
+the same launch configuration the benchmark times, checked on all tokens where
+the oracle is quick (1, 2, 5) and on sampled tokens otherwise (3, 4).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import sparse_mla_decode_combine_gb300 as pkg
+from gpu_util import compare_decode, full_config, need_gpu, small
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode(w: synth.Workload, guard: bool = True):
+    d = synth.to_device(w, "cuda")
+    T, H = w.num_tokens, w.num_heads
+    pad = 64
+    out_full = torch.full((T * H * 512 + 2 * pad,), -7.0, dtype=torch.bfloat16, device="cuda")
+    lse_full = torch.full((T * H + 2 * pad,), -7.0, dtype=torch.float32, device="cuda")
+    out = out_full[pad:pad + T * H * 512].view(T, H, 512)
+    lse = lse_full[pad:pad + T * H].view(T, H)
+    ws = pkg.workspace_for(T, H, w.topk_width, w.window)
+    ws.fill_(0xA5)   # stale workspace contents must not matter
+    pkg.check(pkg.dsv4_sparse_mla_decode(out=out, lse=lse, workspace=ws, **d), "decode")
+    torch.cuda.synchronize()
+    status = pkg.dsv4_get_device_status()
+    if guard:
+        of = out_full.float().cpu().numpy()
+        lf = lse_full.cpu().numpy()
+        assert np.all(of[:pad] == -7.0) and np.all(of[-pad:] == -7.0), "write outside out"
+        assert np.all(lf[:pad] == -7.0) and np.all(lf[-pad:] == -7.0), "write outside lse"
+    return out, lse, status
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_decode_small_configs(n):
+    need_gpu()
+    w = small(n)
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    ref_out, ref_lse, bad = oracle.sparse_mla_decode(w)
+    assert bad == 0
+    compare_decode(out, lse, ref_out, ref_lse, what=w.name)
+
+
+@pytest.mark.parametrize("n", [1, 2, 5])
+def test_decode_full_configs_all_tokens(n):
+    need_gpu()
+    w = full_config(n)
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(w)
+    compare_decode(out, lse, ref_out, ref_lse, what=w.name)
+
+
+@pytest.mark.parametrize("n", [3, 4])
+def test_decode_full_configs_sampled_tokens(n):
+    need_gpu()
+    w = full_config(n)
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    rng = np.random.default_rng(100 + n)
+    rows = np.sort(rng.choice(w.num_tokens, size=12, replace=False))
+    rows[0], rows[-1] = 0, w.num_tokens - 1
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(w, tokens=rows)
+    compare_decode(out, lse, ref_out, ref_lse, rows=rows, what=w.name)
+    # every token: finite output, LSE above the largest single logit's share
+    assert torch.isfinite(out.float()).all()
+
+
+def _edge_workload(heads, sink, window=16, seqs=(1, 0, 2, 5, 300, 129, 64, 65), topk_width=40, seed=77):
+    return synth.make_workload(name="edge", seed=seed, heads=heads, req_seq_lens=list(seqs), topk_width=topk_width,
+                               window=window, sink=sink)
+
+
+@pytest.mark.parametrize("heads", [16, 32, 64, 128])
+@pytest.mark.parametrize("sink", [False, True])
+def test_decode_edge_lengths(heads, sink):
+    """Tokens with an empty history, a single key, keys only in the window, ragged tiles."""
+    need_gpu()
+    w = _edge_workload(heads, sink)
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(w)
+    compare_decode(out, lse, ref_out, ref_lse, what=f"edge h={heads} sink={sink}")
+
+
+def test_decode_window_only_and_topk_only():
+    need_gpu()
+    w = small(5)
+    w0 = synth.Workload(**{**w.__dict__, "topk_lens": np.zeros(w.num_tokens, dtype=np.int32)})
+    out, lse, _ = run_decode(w0)
+    r = oracle.sparse_mla_decode(w0)
+    compare_decode(out, lse, r[0], r[1], what="window only")
+    w1 = synth.Workload(**{**w.__dict__, "window": 0})
+    out, lse, _ = run_decode(w1)
+    r = oracle.sparse_mla_decode(w1)
+    compare_decode(out, lse, r[0], r[1], what="top-k only")
+
+
+def test_decode_many_tokens_no_split():
+    """Enough tokens that every token runs in one worker (no merge)."""
+    need_gpu()
+    rng = np.random.default_rng(5)
+    seqs = rng.integers(100, 600, size=400)
+    w = synth.make_workload(name="many", seed=9, heads=32, req_seq_lens=seqs, topk_width=48, window=16, sink=True)
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    rows = np.arange(0, 400, 7)
+    r = oracle.sparse_mla_decode(w, tokens=rows)
+    compare_decode(out, lse, r[0], r[1], rows=rows, what="many tokens")
+
+
+def test_decode_padded_q_rows_and_repeat_determinism():
+    need_gpu()
+    w = small(2)
+    d = synth.to_device(w, "cuda")
+    T, H = w.num_tokens, w.num_heads
+    qpad = torch.zeros((T, H * 576 + 64), dtype=torch.bfloat16, device="cuda")
+    qpad[:, :H * 576] = d["q"].reshape(T, H * 576)
+    d["q"] = qpad[:, :H * 576].view(T, H, 576)
+    assert d["q"].stride(0) == H * 576 + 64
+    o1, l1 = pkg.sparse_mla_decode(**d)
+    o2, l2 = pkg.sparse_mla_decode(**d)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    r = oracle.sparse_mla_decode(w)
+    compare_decode(o1, l1, r[0], r[1], what="padded q")
+
+
+def test_decode_bad_block_table_entry_sets_status():
+    need_gpu()
+    w = small(4)
+    t = 0
+    pos = int(w.seq_lens[t]) - 1
+    bt = w.block_table.copy()
+    row = int(w.req_idx[t])
+    bt[row, pos // w.page] = w.num_blocks + 5      # out of range under token 0's window
+    wb = synth.Workload(**{**w.__dict__, "block_table": bt})
+    pkg.dsv4_get_device_status()                   # clear
+    out, lse, status = run_decode(wb)
+    assert status == pkg.DSV4_ERR_BAD_INDEX
+    assert pkg.dsv4_get_device_status() == pkg.DSV4_OK   # cleared by the read
+    r = oracle.sparse_mla_decode(wb)
+    assert r[2] > 0
+    compare_decode(out, lse, r[0], r[1], what="bad block table entry (keys skipped)")
+
+
+def test_decode_rejects_bad_arguments():
+    need_gpu()
+    w = small(2)
+    d = synth.to_device(w, "cuda")
+    T, H = w.num_tokens, w.num_heads
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    need = pkg.dsv4_sparse_mla_decode_workspace_size(T, H, w.topk_width, w.window)
+    small_ws = torch.empty(need - 1, dtype=torch.uint8, device="cuda")
+    assert pkg.dsv4_sparse_mla_decode(out=out, lse=lse, workspace=small_ws, **d) == pkg.DSV4_ERR_INVALID_ARG
+    ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    assert pkg.dsv4_sparse_mla_decode(out=out, lse=lse, workspace=ws[1:need + 1], **d) == pkg.DSV4_ERR_INVALID_ARG
+    assert pkg.dsv4_sparse_mla_decode_workspace_size(T, 48, w.topk_width, w.window) == 0

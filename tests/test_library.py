@@ -1,0 +1,68 @@
+"""CPU-only checks of the CUDA library: it builds for sm_103a, loads, exports every
+entry point that include/dsv4.h declares, and rejects bad arguments on the host
+before touching the GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import sparse_mla_decode_combine_gb300 as pkg
+from sparse_mla_decode_combine_gb300 import build as b
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "dsv4.h")).read()
+    return sorted(set(re.findall(r"DSV4_API\s+[\w\s\*]+?\b(dsv4_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    b.build()
+    return pkg.load_library()
+
+
+def test_header_declares_the_abi():
+    syms = declared_symbols()
+    for name in pkg.EXPORTED:
+        assert name in syms
+    assert set(syms) == set(pkg.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", pkg.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (dsv4_\w+)", out))
+    for name in declared_symbols():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_library_is_built_for_sm103a(lib):
+    out = subprocess.run(["cuobjdump", "--list-elf", pkg.library_path()], capture_output=True, text=True).stdout
+    assert "sm_103a" in out
+
+
+def test_host_side_argument_errors(lib):
+    S = None
+    # combine: negative token count, oversize top-k, too narrow output
+    assert lib.dsv4_combine_topk_swa_indices(None, 0, 0, None, None, -1, 0, None, 0, 0, None, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert lib.dsv4_combine_topk_swa_indices(None, 9000, 9000, None, None, 1, 0, None, 0, 9000, None, S) == pkg.DSV4_ERR_UNSUPPORTED
+    assert lib.dsv4_combine_topk_swa_indices(None, 4, 4, None, ctypes.c_void_p(16), 1, 8, None, 12, 11, None, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert lib.dsv4_combine_topk_swa_indices(None, 4, 4, None, None, 0, 8, None, 12, 12, None, S) == pkg.DSV4_OK
+    # decode: unsupported head count, non-finite scale, missing pointers
+    args = [None, 576 * 16, None, 1, 64, None, 1, 1, 1, None, None, 0, 0, None, ctypes.c_void_p(16), 1, 16, 8, None,
+            1.0, None, None, None, 0, S]
+    bad = list(args)
+    bad[16] = 48
+    assert lib.dsv4_sparse_mla_decode(*bad) == pkg.DSV4_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[19] = float("nan")
+    assert lib.dsv4_sparse_mla_decode(*bad) == pkg.DSV4_ERR_INVALID_ARG
+    assert lib.dsv4_sparse_mla_decode(*args) == pkg.DSV4_ERR_INVALID_ARG
+    bad = list(args)
+    bad[15] = 0
+    assert lib.dsv4_sparse_mla_decode(*bad) == pkg.DSV4_OK   # nothing to do
