@@ -12,8 +12,9 @@ ours: inputs resident in HBM; K steps replayed from CUDA graphs, each step on
 one of R replicas of the whole workload (cache pages, block tables, queries,
 outputs) so the bytes the timed steps gather exceed 4x the L2; CUDA events on
 the launching stream, barrier + synchronize on both sides, max over ranks.
-Per-kernel durations for the roofline come from CUPTI kernel records (torch
-profiler) over one extra replay.  e2e repeats the step through the same C ABI
+The roofline divides the algorithmic bytes (or FLOPs) of a step by the CUDA-event
+time of the whole decode call; per-kernel shares come from the committed ncu launch
+list (CUPTI kernel records are not available on the GPU machines).  e2e repeats the step through the same C ABI
 from pinned host buffers with the host<->device copies inside the timed region.
 N > 1: every rank decodes its own batch on its own GPU (no data-path
 collective; weak scaling).
@@ -59,6 +60,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--replicas", type=int, default=0,
+                    help="workload replicas to rotate through (default: enough for 4x the L2)")
     return ap.parse_args()
 
 
@@ -232,25 +235,13 @@ def run_reference(args):
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
-def kernel_times_cupti(replay, names_of_interest=("decode", "combine", "merge")):
-    """Average device duration (us) and count of each of our kernels over one replay()."""
-    import torch
-    from torch.profiler import ProfilerActivity, profile
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        replay()
-        torch.cuda.synchronize()
-    stats = {}
-    for ev in prof.events():
-        name = ev.name
-        if not any(k in name for k in names_of_interest):
-            continue
-        dur = getattr(ev, "device_time", None)
-        if dur is None:
-            dur = getattr(ev, "cuda_time", 0.0)
-        s = stats.setdefault(name, [0, 0.0])
-        s[0] += 1
-        s[1] += float(dur)
-    return {k: {"launches": v[0], "avg_us": v[1] / max(1, v[0])} for k, v in stats.items()}
+def ncu_shares():
+    """Per-kernel time shares of one decode step from the committed ncu launch-list summary."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "launch_shares.json")) as f:
+            return json.load(f)
+    except Exception:
+        return None
 
 
 def traffic_record(kernel_key: str, workload: str):
@@ -308,6 +299,8 @@ def run_ours(args):
     cache_bytes = base["kv_cache"].numel()
     R = max(2, math.ceil(4 * l2 / max(1, bytes_per_step)))
     R = int(min(R, max(2, (24 << 30) // max(1, cache_bytes))))
+    if args.replicas > 0:
+        R = args.replicas
     nb = w.num_blocks
     pool = torch.empty((R * nb, w.page, 656), dtype=torch.uint8, device=dev)
     bts, qs, outs, lses = [], [], [], []
@@ -392,47 +385,32 @@ def run_ours(args):
 
     value = world * T * args.steps / (ms / 1e3)
 
-    # per-kernel device durations (CUPTI) over one rotation of direct calls (the same launches the
-    # graphs hold), for the roofline and the launch count
-    def one_rotation():
-        with torch.cuda.stream(stream):
-            for i in range(G):
-                step(i)
-    try:
-        kt = kernel_times_cupti(one_rotation)
-    except Exception as e:  # profiler unavailable: no roofline numbers
-        kt = {"error": str(e)}
-    launches_per_step = sum(v["launches"] for v in kt.values() if isinstance(v, dict)) / G if "error" not in kt else None
-    decode_name = None
-    if "error" not in kt:
-        dec = {k: v for k, v in kt.items() if "decode" in k}
-        if dec:
-            decode_name = max(dec, key=lambda k: dec[k]["avg_us"] * dec[k]["launches"])
+    # roofline of the decode call, timed with CUDA events over the timed region (the call is the
+    # combine kernel and the decode kernel, plus the merge kernel on the CUDA-core path)
+    launches_per_step = 2 if H >= 64 else 3
     hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
-    roofline = None
-    if decode_name is not None:
-        dur_s = kt[decode_name]["avg_us"] * 1e-6
-        achieved = bytes_per_step / dur_s / 1e9
-        t_hbm = bytes_per_step / (hbm_peak * 1e9)
-        t_tc = flops_per_step / (bf16_peak * 1e12)
-        bound = "hbm" if t_hbm >= t_tc else "tensor"
-        if bound == "hbm":
-            roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                        "frac": achieved / hbm_peak}
-        else:
-            ach_t = flops_per_step / dur_s / 1e12
-            roofline = {"bound": "tensor", "achieved": ach_t, "peak": bf16_peak, "unit": "TFLOP/s",
-                        "frac": ach_t / bf16_peak}
-        m = re.search(r"(\w+_kernel)", decode_name)
-        roofline.update({"traffic": traffic_record(m.group(1) if m else decode_name, w.name),
-                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
-                         "kernel": decode_name, "kernel_avg_us": kt[decode_name]["avg_us"],
-                         "kernel_time_method": "CUPTI kernel records (torch.profiler) over one graph replay of "
-                                               f"{G} steps",
-                         "algorithmic_bytes_per_launch": bytes_per_step, "flops_per_launch": flops_per_step,
-                         "step_roofline_frac": max(t_hbm, t_tc) / (ms / 1e3 / args.steps),
-                         "kv_gbs_step": bytes_per_step * args.steps / (ms / 1e3) / 1e9,
-                         "tflops_step": flops_per_step * args.steps / (ms / 1e3) / 1e12})
+    call_s = ms / 1e3 / args.steps
+    t_hbm = bytes_per_step / (hbm_peak * 1e9)
+    t_tc = flops_per_step / (bf16_peak * 1e12)
+    if t_hbm >= t_tc:
+        ach = bytes_per_step / call_s / 1e9
+        roofline = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak}
+    else:
+        ach = flops_per_step / call_s / 1e12
+        roofline = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s",
+                    "frac": ach / bf16_peak}
+    decode_kernel = "decode_tc_kernel" if H >= 64 else "decode_simt_kernel"
+    roofline.update({
+        "traffic": traffic_record(decode_kernel, w.name),
+        "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+        "kernel": decode_kernel,
+        "timed": "whole decode call per step (combine kernel + decode kernel with its split merge), CUDA "
+                 "events on the launching stream over the timed region; the decode kernel's own share of the "
+                 "step is in ncu_shares (committed ncu launch list)",
+        "call_us": call_s * 1e6,
+        "algorithmic_bytes_per_launch": bytes_per_step, "flops_per_launch": flops_per_step,
+        "kv_gbs": bytes_per_step / call_s / 1e9, "tflops": flops_per_step / call_s / 1e12,
+        "roofline_us": max(t_hbm, t_tc) * 1e6, "ncu_shares": ncu_shares()})
 
     # end to end through the C ABI from pinned host buffers
     e2e = None
@@ -496,15 +474,15 @@ def run_ours(args):
             cpu = cpu_baseline(w, args.cpu_seconds)
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if H >= 64 else "f32",
                 "data": "synthetic",
                 "config": workload_config(w, {"l2": f"inputs larger than L2: {R} rotating replicas "
                                                     f"({R * bytes_per_step / 1e6:.0f} MB gathered per rotation, "
                                                     f"L2 {l2 / 1e6:.0f} MB)",
                                               "replicas": R, "keys_per_step": keys_per_step}),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": None if launches_per_step is None else int(round(launches_per_step * args.steps)),
-                "kernels": kt, "clocks": clocks}
+                "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
+                "clocks": clocks}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -62,19 +62,43 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
     if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128)
         return false;
     Plan p{};
-    p.path = kPathSimt;
-    p.heads_per_group = num_heads == 16 ? 16 : 32;
+    // 64 / 128 heads: tensor-core kernel, 64 heads per CTA, 128-key blocks, one CTA per SM.
+    // 16 / 32 heads: CUDA-core kernel, all heads in one CTA, 32-key tiles.
+    const bool tc = num_heads >= 64;
+    p.path = tc ? kPathTc : kPathSimt;
+    p.heads_per_group = tc ? 64 : num_heads;
     p.groups = num_heads / p.heads_per_group;
     p.cw = topk_width + window;
-    const int tile = kSimtTile;
+    const int tile = tc ? decode_tc_chunk_keys() : kSimtTile;
     const long long units0 = (long long)(num_tokens > 0 ? num_tokens : 1) * p.groups;
-    const int max_splits = std::max(1, std::min(merge_max_splits(), (p.cw + tile - 1) / tile));
-    int want = (int)std::min<long long>(max_splits, (sms + units0 - 1) / units0);
-    want = std::max(1, want);
-    int chunk = (p.cw + want - 1) / want;
-    chunk = std::max(tile, (chunk + tile - 1) / tile * tile);
-    p.chunk = chunk;
-    p.splits = std::max(1, (p.cw + chunk - 1) / chunk);
+    // tensor-core path: the splits of a token form one thread-block cluster (<= 8 CTAs)
+    const int split_cap = tc ? decode_tc_max_splits() : merge_max_splits();
+    const int max_splits = std::max(1, std::min(split_cap, (p.cw + tile - 1) / tile));
+    // Choose the split count minimising (waves x tiles per worker), counting extra time per
+    // worker for merging when a token is split (half a tile through distributed shared memory,
+    // a whole tile through global partials).
+    double best = 1e300;
+    int best_chunk = std::max(tile, (p.cw + tile - 1) / tile * tile);
+    for (int s = 1; s <= max_splits; ++s) {
+        int chunk = (p.cw + s - 1) / s;
+        chunk = std::max(tile, (chunk + tile - 1) / tile * tile);
+        const int s_eff = std::max(1, (p.cw + chunk - 1) / chunk);
+        if (s_eff > split_cap)
+            continue;
+        const long long units = units0 * s_eff;
+        const int resident = tc ? decode_tc_resident_ctas(s_eff) : sms;
+        if (resident <= 0)
+            continue;
+        const long long waves = (units + resident - 1) / resident;
+        const double merge = s_eff > 1 ? (tc ? 0.5 : 1.0) : 0.0;
+        const double cost = (double)waves * ((double)chunk / tile + merge);
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_chunk = chunk;
+        }
+    }
+    p.chunk = best_chunk;
+    p.splits = std::max(1, (p.cw + p.chunk - 1) / p.chunk);
     p.combine_table_bits = combine_table_bits(topk_width);
 
     size_t off = 0;
@@ -84,7 +108,7 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
     off = align_up(off + sizeof(int32_t) * (size_t)num_tokens, 256);
     p.off_part_o = off;
     p.off_part_ml = off;
-    if (p.splits > 1) {
+    if (p.splits > 1 && !tc) {   // the tensor-core kernel merges its splits in shared memory
         off = align_up(off + sizeof(float) * (size_t)num_tokens * p.splits * num_heads * kLatent, 256);
         p.off_part_ml = off;
         off = align_up(off + sizeof(float) * 2 * (size_t)num_tokens * p.splits * num_heads, 256);
@@ -113,6 +137,23 @@ dsv4_status check_combine_args(const int32_t *topk_idx, int64_t topk_stride, int
 int g_attr_bytes[kMaxDevices][kAttrSlots];
 
 }  // namespace
+
+cudaError_t launch_after_previous(const void *kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                                  const DecodeParams &p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {const_cast<DecodeParams *>(&p)};
+    return cudaLaunchKernelExC(&cfg, kernel, args);
+}
 
 cudaError_t set_smem_once(const void *kernel, int bytes, AttrSlot slot)
 {
@@ -195,7 +236,7 @@ extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_
         return DSV4_ERR_INVALID_ARG;
     if (req_idx == nullptr && num_reqs < num_tokens)
         return DSV4_ERR_INVALID_ARG;
-    if ((long long)max_blocks * page_block > INT_MAX)
+    if ((long long)max_blocks * page_block > INT_MAX || (long long)num_blocks * page_block > INT_MAX)
         return DSV4_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(workspace, 256))
         return DSV4_ERR_INVALID_ARG;
@@ -244,8 +285,8 @@ extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_
                                    reinterpret_cast<int32_t *>(ws + pl.off_combined), pl.cw, pl.cw,
                                    reinterpret_cast<int32_t *>(ws + pl.off_lens), pl.combine_table_bits, s);
     if (e == cudaSuccess)
-        e = launch_decode_simt(p, s);
-    if (e == cudaSuccess)
+        e = pl.path == kPathTc ? launch_decode_tc(p, s) : launch_decode_simt(p, s);
+    if (e == cudaSuccess && pl.path == kPathSimt)   // the tensor-core kernel merges its own splits
         e = launch_merge(p, s);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }

@@ -33,6 +33,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t *__rest
                                                            int combined_width, int32_t *__restrict__ combined_lens,
                                                            int bits)
 {
+    // the decode kernel that follows may start its own prologue now; it reads this
+    // kernel's results only after waiting for the whole grid
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ int32_t sm[];
     const int table = 1 << bits;
     int32_t *hkey = sm;           // position stored in the slot, -1 = empty

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_simt_kernel(const DecodePa
     const int t = unit / (p.splits * p.groups);
     const int h0 = group * HG;
 
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // combined lists from the combine kernel
     const int L = p.lens[t];
     const int kbeg = split * p.chunk;
     const int kend = min(L, kbeg + p.chunk);
@@ -293,8 +294,8 @@ cudaError_t launch_simt(const DecodeParams &p, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     const long long grid = (long long)p.num_tokens * p.groups * p.splits;
-    decode_simt_kernel<HG><<<(unsigned)grid, kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_after_previous(reinterpret_cast<const void *>(decode_simt_kernel<HG>), (unsigned)grid, kThreads,
+                                 smem, stream, p);
 }
 
 }  // namespace

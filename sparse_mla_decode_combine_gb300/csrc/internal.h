@@ -60,8 +60,8 @@ struct DecodeParams {
     float scale;
     uint16_t *out;             // BF16 [T, H, 512]
     float *lse;                // [T, H] or null
-    float *part_o;             // [T, groups, splits, hpg, 512] when splits > 1
-    float *part_ml;            // [T, groups, splits, hpg, 2]   (running max, running sum)
+    float *part_o;             // CUDA-core path with splits > 1: [T, groups, splits, hpg, 512]
+    float *part_ml;            // CUDA-core path with splits > 1: [T, groups, splits, hpg, 2] (max, sum)
     int32_t groups;
     int32_t heads_per_group;
     int32_t splits;
@@ -82,8 +82,18 @@ cudaError_t launch_combine(const int32_t *topk, int64_t topk_stride, int topk_wi
                            int64_t combined_stride, int combined_width, int32_t *combined_lens, int table_bits,
                            cudaStream_t stream);
 
+// Launches `kernel(p)` so that it may start while the previous kernel in the stream
+// finishes (programmatic dependent launch); the kernel waits for that kernel's results
+// with griddepcontrol.wait before reading them.
+cudaError_t launch_after_previous(const void *kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                                  const DecodeParams &p);
+
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
+int decode_tc_chunk_keys();
+int decode_tc_max_splits();
+int decode_tc_resident_ctas(int splits);
 int merge_max_splits();
 
 }  // namespace dsv4

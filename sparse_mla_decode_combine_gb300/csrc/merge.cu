@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const DecodeParams p)
 {
     __shared__ float s_w[kMaxSplits];
     __shared__ float s_f;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // partials from the decode kernel
     const int t = blockIdx.x / p.num_heads;
     const int h = blockIdx.x % p.num_heads;
     const int group = h / p.heads_per_group;
@@ -88,8 +89,7 @@ cudaError_t launch_merge(const DecodeParams &p, cudaStream_t stream)
     if (p.splits > kMaxSplits)
         return cudaErrorInvalidValue;
     const long long grid = (long long)p.num_tokens * p.num_heads;
-    merge_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_after_previous(reinterpret_cast<const void *>(merge_kernel), (unsigned)grid, kThreads, 0, stream, p);
 }
 
 }  // namespace dsv4
