@@ -173,6 +173,38 @@ DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_token_strid
                                    dsv4_stream_t stream);
 
 /*
+ * dsv4_sparse_mla_decode_noalloc -- dsv4_sparse_mla_decode without a workspace argument.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory when they decode: code replaying a pipeline whose memory was
+ * fixed at set-up, plug-ins whose host framework owns every allocation, and runtimes that
+ * forbid cudaMalloc between start-up and shutdown.  It computes exactly what
+ * dsv4_sparse_mla_decode computes, with the same arguments except `workspace` and
+ * `workspace_bytes`: the scratch comes from one static device array inside the library,
+ * 16 MiB (16,777,216 bytes), which every GPU that loads the library holds until the process
+ * exits.  Nothing is allocated in the call.
+ *
+ * - A batch whose dsv4_sparse_mla_decode_workspace_size(...) exceeds 16 MiB is rejected with
+ *   DSV4_ERR_UNSUPPORTED before anything is enqueued; use dsv4_sparse_mla_decode for it.
+ * - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *   make that first call before any stream capture on that device.
+ * - All calls on a device share the one array and leave their scratch in it.  Nothing in it
+ *   needs to start at zero (each call writes every scratch value before reading it), but
+ *   calls whose work overlaps on the GPU -- on different streams, or on one stream without
+ *   ordering -- race on the array; serialise them.
+ * Returns the same codes as dsv4_sparse_mla_decode, plus DSV4_ERR_UNSUPPORTED for a batch
+ * too large for the array and DSV4_ERR_CUDA when the address lookup fails.
+ */
+DSV4_API dsv4_status dsv4_sparse_mla_decode_noalloc(const void *q, int64_t q_token_stride, const void *kv_cache,
+                                                   int32_t num_blocks, int32_t page_block, const int32_t *block_table,
+                                                   int64_t bt_stride, int32_t max_blocks, int32_t num_reqs,
+                                                   const int32_t *req_idx, const int32_t *topk_idx,
+                                                   int64_t topk_stride, int32_t topk_width, const int32_t *topk_lens,
+                                                   const int32_t *seq_lens, int32_t num_tokens, int32_t num_heads,
+                                                   int32_t window, const float *sink, float softmax_scale, void *out,
+                                                   float *lse, dsv4_stream_t stream);
+
+/*
  * dsv4_get_device_status -- synchronise `stream`, then read and clear the current
  * device's sticky status word.
  *
