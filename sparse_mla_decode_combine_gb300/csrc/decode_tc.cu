@@ -21,16 +21,19 @@
 //
 // CTA = 512 threads, one (token, 64-head group, split):
 //   warp 0       tcgen05.alloc/dealloc; lane 0 issues the MMAs and commits
-//   warps 1-3    block-table lookups two blocks ahead; loaders
-//   warps 4-7    softmax: thread i owns TMEM lane i = key i of the block (S^T row),
-//                later the value dims of O^T rows; per-head block maxima with
+//   warps 1-15   workers: 16-byte streaming loads of the next block's entries into
+//                registers while the current block computes, then the exact dequant
+//                (E4M3 -> f16 -> f32 * 2^(e-127) -> BF16) into the swizzled K tile;
+//                warps 1-3 also look up cache slots two blocks ahead
+//   warps 4-11   also the softmax: lane i of a warp owns TMEM lane i of its quadrant
+//                (key i of the block in S^T, a value dim in O^T), two warps per
+//                quadrant split the 64 heads; per-head block maxima with
 //                redux.sync.max.f32, lazy rescaling (only when a head's max grows by
 //                more than 2^8), P^T (BF16) into shared memory, row sums in TMEM
-//   warps 1-3,8-15 loaders: 16-byte streaming loads of the next block's entries into
-//                registers while the current block computes; exact dequant
-//                (E4M3 -> f16 -> f32 * 2^(e-127) -> BF16) into the swizzled K tile
 // When a token's keys are split over S CTAs (S <= 8), the S CTAs form a thread-block
-// cluster and merge their partial results through distributed shared memory.
+// cluster: each stages its partial in its own shared memory and, after a cluster
+// barrier, every CTA merges a slice of the heads by reading its peers' partials
+// through distributed shared memory.
 // Every mbarrier wait is bounded; a wait that runs out records DSV4_ERR_TIMEOUT in
 // the status word and the CTA finishes without waiting again.
 #include <cuda_bf16.h>
@@ -51,11 +54,12 @@ constexpr int kQBytes = kChunks * kNH * 128;     // 73728
 constexpr int kKBytes = kChunks * kBK * 128;     // 147456
 constexpr int kChunkBytes = kBK * 128;           // 16384 (one 64-dim column chunk of the K tile)
 constexpr int kQChunkBytes = kNH * 128;          // 8192
-constexpr int kLoaders = 352;                    // warps 1-3 and 8-15
-constexpr int kPieces = 41;                      // 16-byte pieces per entry
-constexpr int kRowGroups = 8;                    // loader lt < 328 owns piece lt % 41 of rows lt / 41 + 8 i
-constexpr int kActiveLoaders = kPieces * kRowGroups;   // 328
-constexpr int kRowsPerLoader = kBK / kRowGroups;       // 16
+constexpr int kWorkers = 480;                    // warps 1-15: loads + dequant (and softmax on warps 4-11)
+constexpr int kDataPieces = 40;                  // 16-byte pieces per entry holding data (32 latent + 8 rope)
+constexpr int kRowGroups = kWorkers / kDataPieces;     // 12: worker w owns piece w % 40 of rows w / 40 + 12 i
+constexpr int kRowsPerLoader = (kBK + kRowGroups - 1) / kRowGroups;   // 11
+constexpr int kSoftWarps = 8;            // two per TMEM lane quadrant, 32 heads each
+constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;            // S^T: 64 columns
 constexpr uint32_t kColO = 64;           // O^T: 4 tiles x 64 columns
@@ -188,17 +192,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
                  : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-                 "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-                 "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-                 : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -288,21 +281,33 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
 {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // Split-KV merge inside a cluster of S = splits CTAs (one per split of a token's keys).
-// Head h is owned by rank h / hp (hp = ceil(64 / S)).  After the first cluster barrier
-// every CTA pushes, into the owner's (now idle) shared memory, its running max m_s
-// (natural-log units) and row sum l_s per head (stat region, [S][hp] each) and its
-// unnormalised O_s rows (partial region, [S][hp][512] fp32).  After the second barrier
-// each owner merges its heads from local memory:
+// Every CTA has staged, in its own shared memory, its running max m_s (natural-log
+// units, s_m[h]) and row sum l_s (s_l[h]) per head and its unnormalised O_s as fp32
+// [64 heads][512] (s_o).  After a cluster barrier the CTA of rank r merges heads
+// [r*hp, (r+1)*hp) (hp = ceil(64 / S)), reading all S partials through distributed
+// shared memory with the loads of all splits in flight together:
 //   m = max(max_s m_s, sink), Z = sum_s l_s e^{m_s - m} + e^{sink - m},
 //   out = sum_s e^{m_s - m} O_s / Z  (BF16),  lse = m + ln Z.
-__device__ void cluster_merge_owned(const DecodeParams &p, int t, int h0, int rank, const float *st_m,
-                                    const float *st_l, const float *part, float *wts)
+__device__ void cluster_merge_pull(const DecodeParams &p, int t, int h0, int rank, uint32_t s_m, uint32_t s_l,
+                                   uint32_t s_o, float *wts)
 {
     const int S = p.splits;
     const int hp = (kNH + S - 1) / S;
@@ -310,43 +315,59 @@ __device__ void cluster_merge_owned(const DecodeParams &p, int t, int h0, int ra
     const int he = min(kNH, hb + hp);
     const int tid = threadIdx.x;
     if (tid < he - hb) {
+        const int h = hb + tid;
+        float ms[kMaxSplits], ls[kMaxSplits];
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s) {
+            ms[s] = s < S ? ld_cluster_f32(map_to_rank(s_m + 4u * h, s)) : -INFINITY;
+            ls[s] = s < S ? ld_cluster_f32(map_to_rank(s_l + 4u * h, s)) : 0.f;
+        }
         float m = -INFINITY;
-        for (int s = 0; s < S; ++s)
-            m = fmaxf(m, st_m[s * hp + tid]);
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s)
+            m = fmaxf(m, ms[s]);
         const float mk = m;
         float sk = 0.f;
         if (p.sink != nullptr) {
-            sk = p.sink[h0 + hb + tid];
+            sk = p.sink[h0 + h];
             m = fmaxf(m, sk);
         }
         float z = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const float ms = st_m[s * hp + tid];
-            z += ms == -INFINITY ? 0.f : st_l[s * hp + tid] * expf(ms - m);
+        float w[kMaxSplits];
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s) {
+            w[s] = ms[s] == -INFINITY ? 0.f : expf(ms[s] - m);
+            z += ls[s] * w[s];
         }
         if (p.sink != nullptr)
             z += expf(sk - m);
         const float f = (z > 0.f && mk != -INFINITY) ? 1.f / z : 0.f;
-        for (int s = 0; s < kMaxSplits; ++s) {
-            const float ms = s < S ? st_m[s * hp + tid] : -INFINITY;
-            wts[tid * 10 + s] = ms != -INFINITY ? expf(ms - m) * f : 0.f;
-        }
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s)
+            wts[tid * 10 + s] = w[s] * f;
         wts[tid * 10 + 8] = z > 0.f ? m + logf(z) : -INFINITY;
     }
     __syncthreads();
+    uint32_t peer[kMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+        peer[s] = s < S ? map_to_rank(s_o, s) : 0u;
     for (int i = tid; i < (he - hb) * (kLatent / 4); i += kThreads) {
         const int hl = i / (kLatent / 4);
         const int c = i % (kLatent / 4);
+        const uint32_t off = (uint32_t)((hb + hl) * kLatent + 4 * c) * 4u;
+        float4 v[kMaxSplits];
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s)
+            v[s] = (s < S && wts[hl * 10 + s] != 0.f) ? ld_cluster_v4(peer[s] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < S; ++s) {
-            const float w = wts[hl * 10 + s];
-            if (w == 0.f)
-                continue;
-            const float4 v = *reinterpret_cast<const float4 *>(part + ((size_t)(s * hp + hl) * kLatent + 4 * c));
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s) {
+            const float ws = wts[hl * 10 + s];
+            acc.x = fmaf(ws, v[s].x, acc.x);
+            acc.y = fmaf(ws, v[s].y, acc.y);
+            acc.z = fmaf(ws, v[s].z, acc.z);
+            acc.w = fmaf(ws, v[s].w, acc.w);
         }
         uint2 u;
         u.x = pack_bf16x2(acc.x, acc.y);
@@ -356,19 +377,6 @@ __device__ void cluster_merge_owned(const DecodeParams &p, int t, int h0, int ra
         if (c == 0 && p.lse != nullptr)
             p.lse[(int64_t)t * p.num_heads + h] = wts[hl * 10 + 8];
     }
-}
-
-// Remote addresses for pushing this split's per-head results to their owners:
-// hadr[h] = partial row of head h in its owner, madr/ladr[h] = its stat slots.
-__device__ __forceinline__ void owner_addresses(int S, int split, uint32_t s_part, uint32_t s_stm, uint32_t s_stl,
-                                                int h, uint32_t *hadr, uint32_t *madr, uint32_t *ladr)
-{
-    const int hp = (kNH + S - 1) / S;
-    const int owner = h / hp;
-    const int slot = split * hp + (h - owner * hp);
-    hadr[h] = map_to_rank(s_part + (uint32_t)slot * kLatent * 4u, (uint32_t)owner);
-    madr[h] = map_to_rank(s_stm + (uint32_t)slot * 4u, (uint32_t)owner);
-    ladr[h] = map_to_rank(s_stl + (uint32_t)slot * 4u, (uint32_t)owner);
 }
 
 // Logical position of key `k` of block `b` -> cache slot (phys_block * page + offset), or -1.
@@ -426,21 +434,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     float *red = reinterpret_cast<float *>(small + kOffRed);
     float *mrun = reinterpret_cast<float *>(small + kOffMrun);
     float *mcs = reinterpret_cast<float *>(small + kOffMc);
-    float *alpha = reinterpret_cast<float *>(small + kOffAlpha);   // also this split's max per head (merge)
-    float *fin = reinterpret_cast<float *>(small + kOffFin);       // also this split's row sum per head (merge)
+    float *alpha = reinterpret_cast<float *>(small + kOffAlpha);   // at the end: this split's max per head
+    float *fin = reinterpret_cast<float *>(small + kOffFin);       // at the end: this split's row sum per head
     const uint32_t bar_s = smem_u32(small + kOffBars);
     const uint32_t bar_p = bar_s + 8;
     const uint32_t bar_o = bar_s + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small + kOffTmem);
     volatile int *flags = reinterpret_cast<volatile int *>(small + kOffFlags);   // [0] abort, [1] rescale block tag
-    // merge (Q and K-tile regions are idle by then): stats [S][hp] x 2, weights, addresses; partials in K tile
-    float *st_m = reinterpret_cast<float *>(gbase);
-    float *st_l = reinterpret_cast<float *>(gbase + 2048);
-    float *wts = reinterpret_cast<float *>(gbase + 4096);
-    uint32_t *hadr = reinterpret_cast<uint32_t *>(gbase + 8192);
-    uint32_t *madr = hadr + kNH;
-    uint32_t *ladr = hadr + 2 * kNH;
-    float *part = reinterpret_cast<float *>(gbase + kQBytes);
+    float *wts = reinterpret_cast<float *>(gbase + 40960);   // merge weights (Q region, idle at the end)
+    float *o_stage = reinterpret_cast<float *>(gbase + kQBytes);   // partial O [64][512] fp32 (K tile region)
 
     grid_dependency_wait();   // combined lists and lengths are ready
 
@@ -467,25 +469,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             }
             return;
         }
-        cluster_sync();   // every CTA of the cluster is past its main loop
         if (tid < kNH) {   // an empty partial: weight 0 in the merge, its O is never read
-            owner_addresses(p.splits, split, sK, smem_u32(st_m), smem_u32(st_l), tid, hadr, madr, ladr);
-            st_cluster_f32(madr[tid], -INFINITY);
-            st_cluster_f32(ladr[tid], 0.f);
+            alpha[tid] = -INFINITY;
+            fin[tid] = 0.f;
         }
-        cluster_sync();   // all partials are in place
-        cluster_merge_owned(p, t, h0, split, st_m, st_l, part, wts);
+        cluster_sync();   // every split has staged its partial
+        cluster_merge_pull(p, t, h0, split, smem_u32(alpha), smem_u32(fin), sK, wts);
+        cluster_sync();   // peers have finished reading this CTA's shared memory
         return;
     }
 
     const bool is_mma = warp == 0;
-    const bool is_soft = warp >= 4 && warp < 8;
-    const bool is_loader = !is_mma && !is_soft;
-    const int lt = warp < 4 ? tid - 32 : tid - 160;   // loader index 0..351
+    const bool is_soft = warp >= 4 && warp < 4 + kSoftWarps;
+    const int wk = tid - 32;                              // worker index 0..479 (warps 1-15)
+    const int stid = tid - 128;                           // softmax thread index 0..255 (warps 4-11)
+    const int quad = warp & 3;                            // TMEM lane quadrant of this warp
+    const int hh = (warp - 4) >> 2;                       // softmax: head half (heads 32 hh .. 32 hh + 31)
+    const int key = quad * 32 + lane;                     // softmax: key of the block / value dim of a tile
 
     if (tid == 0) {
         mbar_init(bar_s, 1);
-        mbar_init(bar_p, 4);
+        mbar_init(bar_p, kSoftWarps);
         mbar_init(bar_o, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         flags[0] = 0;
@@ -515,76 +519,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     __syncthreads();
     tc_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);   // this warp's TMEM lanes
 
-    const uint32_t soft_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this softmax warp's TMEM lanes
-    const int key = tid - 128;                                              // softmax: key / dv row index
-
-    // Role loops.  Per block b the three roles meet once at named barrier 3 (all 512
-    // threads: the K tile of block b is complete); everything else is ordered by the
-    // mbarriers S-full (QK^T done), P-full (P^T written) and O-done (P.V done).
-    if (is_loader) {
-        // loader lt (< 328) owns 16-byte piece `pc` of rows rg, rg + 8, ..., rg + 120 of every block
-        const bool active = lt < kActiveLoaders;
-        const int pc = lt % kPieces;
-        const int rg = lt / kPieces;
-        uint4 pre[kRowsPerLoader];
-        auto issue_loads = [&](int b) {
-            const int *sl = slots + (b % 3) * kBK + rg;
-#pragma unroll
-            for (int it = 0; it < kRowsPerLoader; ++it) {
-                const int sidx = active ? sl[kRowGroups * it] : -1;
-                pre[it] = sidx >= 0 ? ld_stream(p.kv + (int64_t)sidx * kEntryBytes + 16 * pc) : make_uint4(0, 0, 0, 0);
-            }
-        };
-        // this thread's rows share (row & 7) = rg, so its swizzled offsets differ by 1024 per row step;
-        // neighbouring chunks store their two 16-byte units in opposite order (no bank conflicts)
-        const uint32_t u0 = (uint32_t)(pc & 3) * 2u;
-        const int chunk = pc >> 2;
-        const bool odd = chunk & 1;
-        const uint32_t off_first = (uint32_t)rg * 128u + (((u0 + (odd ? 1u : 0u)) ^ (uint32_t)rg) << 4);
-        const uint32_t off_second = (uint32_t)rg * 128u + (((u0 + (odd ? 0u : 1u)) ^ (uint32_t)rg) << 4);
-        const uint32_t dst_lat = sK + (uint32_t)chunk * kChunkBytes;
-        const uint32_t dst_rope = sK + 8u * kChunkBytes + (uint32_t)rg * 128u + ((((uint32_t)pc - 32u) ^ (uint32_t)rg) << 4);
-        const int scale_shift = 8 * (pc >> 3);
-        issue_loads(0);
-        for (int b = 0; b < nblocks; ++b) {
-            if (b > 0)
-                mbar_wait(bar_o, (uint32_t)((b - 1) & 1), flags, p.status);   // P.V has drained the tile
-            // scale words first (piece 40 of each entry), then the exact dequant into the K tile
-            if (active && pc == 40) {
-#pragma unroll
-                for (int it = 0; it < kRowsPerLoader; ++it)
-                    scal[rg + kRowGroups * it] = pre[it].x;
-            }
-            named_bar(2, kLoaders);
-            if (active && pc < 32) {
-#pragma unroll
-                for (int it = 0; it < kRowsPerLoader; ++it) {
-                    const float sc = ue8m0_to_float((scal[rg + kRowGroups * it] >> scale_shift) & 0xFFu);
-                    const uint4 v = pre[it];
-                    const uint32_t a0 = e4m3x2_to_bf16x2(v.x, sc), a1 = e4m3x2_to_bf16x2(v.x >> 16, sc);
-                    const uint32_t a2 = e4m3x2_to_bf16x2(v.y, sc), a3 = e4m3x2_to_bf16x2(v.y >> 16, sc);
-                    const uint32_t b0 = e4m3x2_to_bf16x2(v.z, sc), b1 = e4m3x2_to_bf16x2(v.z >> 16, sc);
-                    const uint32_t b2 = e4m3x2_to_bf16x2(v.w, sc), b3 = e4m3x2_to_bf16x2(v.w >> 16, sc);
-                    const uint32_t rowbase = dst_lat + (uint32_t)it * 1024u;
-                    st_shared_v4(rowbase + off_first, odd ? b0 : a0, odd ? b1 : a1, odd ? b2 : a2, odd ? b3 : a3);
-                    st_shared_v4(rowbase + off_second, odd ? a0 : b0, odd ? a1 : b1, odd ? a2 : b2, odd ? a3 : b3);
-                }
-            } else if (active && pc < 40) {
-#pragma unroll
-                for (int it = 0; it < kRowsPerLoader; ++it)
-                    st_shared_v4(dst_rope + (uint32_t)it * 1024u, pre[it].x, pre[it].y, pre[it].z, pre[it].w);
-            }
-            fence_async_smem();
-            named_bar(3, kThreads);   // K tile of block b complete
-            if (b + 1 < nblocks)
-                issue_loads(b + 1);
-            if (warp < 4 && b + 2 < nblocks) {
-                for (int k = tid - 32; k < kBK; k += 96)
-                    slots[((b + 2) % 3) * kBK + k] = slot_of(p, t, row, row_ok, kbeg, kend, b + 2, k);
-            }
-        }
-    } else if (is_mma) {
+    if (is_mma) {
         // descriptors: 128-byte swizzle; K-major S^T operands advance 32 B per 16-dim step and one
         // column chunk per 64 dims; MN-major P.V operands advance 2 KB per 16 keys
         const uint64_t qk_a = sdesc(sK, 16, 1024);
@@ -593,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         const uint64_t pv_b = sdesc(sP, 1024, 1024);   // one 64-head group along N: LBO unused, kept = SBO
         for (int b = 0; b < nblocks; ++b) {
             const uint32_t ph = (uint32_t)(b & 1);
-            named_bar(3, kThreads);
+            named_bar(3, kThreads);   // K tile of block b complete
             if (lane == 0) {
                 tc_after();
 #pragma unroll
@@ -617,33 +554,101 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             }
             __syncwarp();
         }
-    } else {   // softmax warps
+    } else {
+        // ---- workers.  Worker wk owns 16-byte piece pc = wk % 40 of rows rg, rg + 12, ... of every
+        // block (pieces 0-31 latent, 32-39 rope); workers 0-127 also fetch the scale word of row wk.
+        const int pc = wk % kDataPieces;
+        const int rg = wk / kDataPieces;
+        const bool latent = pc < 32;
+        const int chunk = latent ? pc >> 2 : 8;
+        const uint32_t u0 = latent ? (uint32_t)(pc & 3) * 2u : (uint32_t)(pc - 32);
+        const bool odd = latent && (chunk & 1);   // neighbouring chunks store their two units in opposite order
+        const int scale_shift = 8 * (pc >> 3);
+        uint4 pre[kRowsPerLoader];
+        unsigned pre_scale = 0;
+        auto issue_loads = [&](int b) {
+            const int *sl = slots + (b % 3) * kBK;
+#pragma unroll
+            for (int it = 0; it < kRowsPerLoader; ++it) {
+                const int r = rg + kRowGroups * it;
+                const int sidx = r < kBK ? sl[r] : -1;
+                pre[it] = sidx >= 0 ? ld_stream(p.kv + (int64_t)sidx * kEntryBytes + 16 * pc) : make_uint4(0, 0, 0, 0);
+            }
+            if (wk < kBK) {
+                const int sidx = sl[wk];
+                pre_scale = sidx >= 0 ? __ldg(reinterpret_cast<const unsigned *>(p.kv + (int64_t)sidx * kEntryBytes +
+                                                                                  kScaleOffset))
+                                      : 0u;
+            }
+        };
+        issue_loads(0);
         for (int b = 0; b < nblocks; ++b) {
             const uint32_t ph = (uint32_t)(b & 1);
-            named_bar(3, kThreads);
-            mbar_wait(bar_s, ph, flags, p.status);
             if (b > 0)
-                mbar_wait(bar_o, ph ^ 1u, flags, p.status);   // O^T and row sums are settled
+                mbar_wait(bar_o, ph ^ 1u, flags, p.status);   // P.V has drained the tile
+            if (wk < kBK)
+                scal[wk] = pre_scale;
+            named_bar(2, kWorkers);
+            // the row addresses are recomputed each block (an opaque copy of rg stops the compiler
+            // from hoisting 22 of them into registers for the whole loop)
+            int rgb = rg;
+            asm volatile("" : "+r"(rgb));
+#pragma unroll
+            for (int it = 0; it < kRowsPerLoader; ++it) {
+                const int r = rgb + kRowGroups * it;
+                if (r >= kBK)
+                    continue;
+                const uint32_t rowbase = sK + (uint32_t)chunk * kChunkBytes + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
+                const uint4 v = pre[it];
+                if (latent) {
+                    const float sc = ue8m0_to_float((scal[r] >> scale_shift) & 0xFFu);
+                    const uint32_t a0 = e4m3x2_to_bf16x2(v.x, sc), a1 = e4m3x2_to_bf16x2(v.x >> 16, sc);
+                    const uint32_t a2 = e4m3x2_to_bf16x2(v.y, sc), a3 = e4m3x2_to_bf16x2(v.y >> 16, sc);
+                    const uint32_t b0 = e4m3x2_to_bf16x2(v.z, sc), b1 = e4m3x2_to_bf16x2(v.z >> 16, sc);
+                    const uint32_t b2 = e4m3x2_to_bf16x2(v.w, sc), b3 = e4m3x2_to_bf16x2(v.w >> 16, sc);
+                    const uint32_t uf = u0 + (odd ? 1u : 0u);
+                    const uint32_t us = u0 + (odd ? 0u : 1u);
+                    st_shared_v4(rowbase + ((uf ^ (uint32_t)(r & 7)) << 4), odd ? b0 : a0, odd ? b1 : a1,
+                                 odd ? b2 : a2, odd ? b3 : a3);
+                    st_shared_v4(rowbase + ((us ^ (uint32_t)(r & 7)) << 4), odd ? a0 : b0, odd ? a1 : b1,
+                                 odd ? a2 : b2, odd ? a3 : b3);
+                } else {
+                    st_shared_v4(rowbase + ((u0 ^ (uint32_t)(r & 7)) << 4), v.x, v.y, v.z, v.w);
+                }
+            }
+            fence_async_smem();
+            named_bar(3, kThreads);   // K tile of block b complete
+            if (b + 1 < nblocks)
+                issue_loads(b + 1);
+            if (warp < 4 && b + 2 < nblocks) {
+                for (int k = tid - 32; k < kBK; k += 96)
+                    slots[((b + 2) % 3) * kBK + k] = slot_of(p, t, row, row_ok, kbeg, kend, b + 2, k);
+            }
+            if (!is_soft)
+                continue;
+            // ---- softmax of block b (warps 4-11; this warp: lanes of its quadrant, heads 32hh..32hh+31)
+            mbar_wait(bar_s, ph, flags, p.status);
             tc_after();
             const bool kv = (b * kBK + key < nkeys) && slots[(b % 3) * kBK + key] >= 0;
-            // per-head maxima of this block (over keys = lanes); the 32 reductions of a column
-            // group are independent, lane j keeps the j-th
-#pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {
-                uint32_t s[32];
-                tmem_ld32(soft_row + kColS + 32 * hc, s);
-                tmem_ld_wait();
+            const uint32_t colS = kColS + 32 * hh;
+            {   // per-head maxima of this block over the 32 keys of the quadrant; lane j keeps head j
                 float mine = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float m = warp_max(kv ? __uint_as_float(s[j]) : -INFINITY);
-                    mine = lane == j ? m : mine;
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t s[16];
+                    tmem_ld16(lane_base + colS + 16 * half, s);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float m = warp_max(kv ? __uint_as_float(s[j]) : -INFINITY);
+                        mine = lane == 16 * half + j ? m : mine;
+                    }
                 }
-                red[(warp & 3) * kNH + 32 * hc + lane] = mine;
+                red[quad * kNH + 32 * hh + lane] = mine;
             }
-            named_bar(1, 128);
-            if (key < kNH) {
-                const int h = key;
+            named_bar(1, kSoftThreads);
+            if (stid < kNH) {
+                const int h = stid;
                 const float mb = fmaxf(fmaxf(red[h], red[kNH + h]), fmaxf(red[2 * kNH + h], red[3 * kNH + h]));
                 const float mo = mrun[h];
                 float mn = mo;
@@ -659,40 +664,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 mcs[h] = mn == -INFINITY ? 0.f : mn * c2;
                 alpha[h] = a;
             }
-            named_bar(1, 128);
+            named_bar(1, kSoftThreads);
             if (flags[1] == b + 1) {   // some head's max grew past the threshold: rescale O^T and row sums
-                uint32_t x[32];
+                uint32_t x[16];
 #pragma unroll 1
-                for (int col = kColO; col < (int)kColL + 64; col += 32) {
-                    const int hb = (col - kColO) & 63;
-                    tmem_ld32(soft_row + col, x);
+                for (int m = 0; m < 10; ++m) {   // four O^T tiles, then the row sums, 16 columns at a time
+                    const uint32_t col = ((m >> 1) < 4 ? kColO + 64 * (m >> 1) : kColL) + 32 * hh + 16 * (m & 1);
+                    tmem_ld16(lane_base + col, x);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        x[j] = __float_as_uint(__uint_as_float(x[j]) * alpha[hb + j]);
-                    tmem_st32(soft_row + col, x);
+                    for (int j = 0; j < 16; ++j)
+                        x[j] = __float_as_uint(__uint_as_float(x[j]) * alpha[32 * hh + 16 * (m & 1) + j]);
+                    tmem_st16(lane_base + col, x);
                 }
             }
             // P = 2^(s*c - m*c) -> BF16 P^T row `key`; row sums accumulate per lane in TMEM
 #pragma unroll 1
-            for (int hq = 0; hq < 4; ++hq) {   // 16 heads at a time
+            for (int hq = 0; hq < 2; ++hq) {   // 16 heads at a time
+                const int hb = 32 * hh + 16 * hq;
                 uint32_t sv[16], l[16];
-                tmem_ld16(soft_row + kColS + 16 * hq, sv);
+                tmem_ld16(lane_base + kColS + hb, sv);
                 if (b > 0)
-                    tmem_ld16(soft_row + kColL + 16 * hq, l);
+                    tmem_ld16(lane_base + kColL + hb, l);
                 tmem_ld_wait();
                 uint32_t pk[8];
 #pragma unroll
                 for (int j = 0; j < 16; j += 2) {
-                    const float p0 = kv ? exp2f(fmaf(__uint_as_float(sv[j]), c2, -mcs[16 * hq + j])) : 0.f;
-                    const float p1 = kv ? exp2f(fmaf(__uint_as_float(sv[j + 1]), c2, -mcs[16 * hq + j + 1])) : 0.f;
+                    const float p0 = kv ? exp2f(fmaf(__uint_as_float(sv[j]), c2, -mcs[hb + j])) : 0.f;
+                    const float p1 = kv ? exp2f(fmaf(__uint_as_float(sv[j + 1]), c2, -mcs[hb + j + 1])) : 0.f;
                     l[j] = __float_as_uint((b > 0 ? __uint_as_float(l[j]) : 0.f) + p0);
                     l[j + 1] = __float_as_uint((b > 0 ? __uint_as_float(l[j + 1]) : 0.f) + p1);
                     pk[j >> 1] = pack_bf16x2(p0, p1);
                 }
-                tmem_st16(soft_row + kColL + 16 * hq, l);
-                st_shared_v4(sP + sw128(key, 2 * hq), pk[0], pk[1], pk[2], pk[3]);
-                st_shared_v4(sP + sw128(key, 2 * hq + 1), pk[4], pk[5], pk[6], pk[7]);
+                tmem_st16(lane_base + kColL + hb, l);
+                st_shared_v4(sP + sw128(key, hb >> 3), pk[0], pk[1], pk[2], pk[3]);
+                st_shared_v4(sP + sw128(key, (hb >> 3) + 1), pk[4], pk[5], pk[6], pk[7]);
             }
             tmem_st_wait();
             fence_async_smem();
@@ -706,21 +712,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     mbar_wait(bar_o, (uint32_t)((nblocks - 1) & 1), flags, p.status);
     tc_after();
 
-    // ---- epilogue: row sums across lanes; normalised output, or the partial pushed for the merge
+    // ---- epilogue: row sums across lanes; normalised output, or the partial staged for the merge
     float *lred = reinterpret_cast<float *>(gbase);   // Q region is free: [128 lanes][65]
     if (is_soft) {
-        uint32_t l[32];
-#pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-            tmem_ld32(soft_row + kColL + 32 * hc, l);
+        {
+            uint32_t l[32];
+            tmem_ld32(lane_base + kColL + 32 * hh, l);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                lred[key * 65 + 32 * hc + j] = __uint_as_float(l[j]);
+                lred[key * 65 + 32 * hh + j] = __uint_as_float(l[j]);
         }
-        named_bar(1, 128);
-        if (key < kNH) {
-            const int h = key;
+        named_bar(1, kSoftThreads);
+        if (stid < kNH) {
+            const int h = stid;
             float acc[8];
 #pragma unroll
             for (int a = 0; a < 8; ++a)
@@ -750,47 +755,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 fin[h] = ms == -INFINITY ? 0.f : lsum;
             }
         }
-        named_bar(1, 128);
-        if (p.splits == 1) {
-            uint32_t x[32];
+        named_bar(1, kSoftThreads);
+        uint32_t x[32];
 #pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
-                const int dv = 128 * m + key;
-#pragma unroll 1
-                for (int hc = 0; hc < 2; ++hc) {
-                    tmem_ld32(soft_row + kColO + 64 * m + 32 * hc, x);
-                    tmem_ld_wait();
+        for (int m = 0; m < 4; ++m) {
+            const int dv = 128 * m + key;
+            tmem_ld32(lane_base + kColO + 64 * m + 32 * hh, x);
+            tmem_ld_wait();
+            if (p.splits == 1) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int h = 32 * hc + j;
-                        p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] =
-                            bf16_bits(__uint_as_float(x[j]) * fin[h]);
-                    }
+                for (int j = 0; j < 32; ++j) {
+                    const int h = 32 * hh + j;
+                    p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] = bf16_bits(__uint_as_float(x[j]) * fin[h]);
                 }
-            }
-        }
-    }
-    if (p.splits > 1) {
-        cluster_sync();   // every CTA of the cluster is past its main loop: Q and K-tile regions are idle
-        if (is_soft) {
-            if (key < kNH) {
-                owner_addresses(p.splits, split, sK, smem_u32(st_m), smem_u32(st_l), key, hadr, madr, ladr);
-                st_cluster_f32(madr[key], alpha[key]);
-                st_cluster_f32(ladr[key], fin[key]);
-            }
-            named_bar(1, 128);
-            uint32_t x[32];
-#pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t dvb = 4u * (uint32_t)(128 * m + key);
-#pragma unroll 1
-                for (int hc = 0; hc < 2; ++hc) {
-                    tmem_ld32(soft_row + kColO + 64 * m + 32 * hc, x);
-                    tmem_ld_wait();
+            } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        st_cluster_f32(hadr[32 * hc + j] + dvb, __uint_as_float(x[j]));
-                }
+                for (int j = 0; j < 32; ++j)
+                    o_stage[(32 * hh + j) * kLatent + dv] = __uint_as_float(x[j]);
             }
         }
     }
@@ -800,8 +781,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     if (is_mma)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     if (p.splits > 1) {
-        cluster_sync();   // all partials are in place
-        cluster_merge_owned(p, t, h0, split, st_m, st_l, part, wts);
+        cluster_sync();   // every split has staged its partial
+        cluster_merge_pull(p, t, h0, split, smem_u32(alpha), smem_u32(fin), sK, wts);
+        cluster_sync();   // peers have finished reading this CTA's shared memory
     }
 }
 
