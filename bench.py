@@ -385,9 +385,9 @@ def run_ours(args):
 
     value = world * T * args.steps / (ms / 1e3)
 
-    # roofline of the decode call, timed with CUDA events over the timed region (the call is the
-    # combine kernel and the decode kernel, plus the merge kernel on the CUDA-core path)
-    launches_per_step = 2 if H >= 64 else 3
+    # roofline of the decode call, timed with CUDA events over the timed region (64/128 heads: one
+    # kernel that combines, decodes and merges; 16/32 heads: combine, decode and merge kernels)
+    launches_per_step = 1 if H >= 64 else 3
     hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
     call_s = ms / 1e3 / args.steps
     t_hbm = bytes_per_step / (hbm_peak * 1e9)

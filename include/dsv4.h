@@ -181,10 +181,10 @@ DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_token_strid
  * forbid cudaMalloc between start-up and shutdown.  It computes exactly what
  * dsv4_sparse_mla_decode computes, with the same arguments except `workspace` and
  * `workspace_bytes`: the scratch comes from one static device array inside the library,
- * 16 MiB (16,777,216 bytes), which every GPU that loads the library holds until the process
+ * 32 MiB (33,554,432 bytes), which every GPU that loads the library holds until the process
  * exits.  Nothing is allocated in the call.
  *
- * - A batch whose dsv4_sparse_mla_decode_workspace_size(...) exceeds 16 MiB is rejected with
+ * - A batch whose dsv4_sparse_mla_decode_workspace_size(...) exceeds 32 MiB is rejected with
  *   DSV4_ERR_UNSUPPORTED before anything is enqueued; use dsv4_sparse_mla_decode for it.
  * - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
  *   make that first call before any stream capture on that device.

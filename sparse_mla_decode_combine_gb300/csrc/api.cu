@@ -69,19 +69,21 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
     p.heads_per_group = tc ? 64 : num_heads;
     p.groups = num_heads / p.heads_per_group;
     p.cw = topk_width + window;
-    const int tile = tc ? decode_tc_chunk_keys() : kSimtTile;
+    const int tile = tc ? decode_tc_block_keys() : kSimtTile;
     const long long units0 = (long long)(num_tokens > 0 ? num_tokens : 1) * p.groups;
     // tensor-core path: the splits of a token form one thread-block cluster (<= 8 CTAs)
     const int split_cap = tc ? decode_tc_max_splits() : merge_max_splits();
     const int max_splits = std::max(1, std::min(split_cap, (p.cw + tile - 1) / tile));
-    // Choose the split count minimising (waves x tiles per worker), counting extra time per
-    // worker for merging when a token is split (half a tile through distributed shared memory,
-    // a whole tile through global partials).
+    // Choose the split count minimising (waves x time per worker).  CUDA-core path: time in
+    // tiles, plus one tile for the global merge when split.  Tensor-core path: a 128-key block
+    // costs its matrix products and softmax whatever its fill, the gather scales with the keys
+    // (chunks are multiples of 16 keys), plus the prologue and, when split, the cluster merge.
+    const int gran = tc ? 16 : tile;
     double best = 1e300;
-    int best_chunk = std::max(tile, (p.cw + tile - 1) / tile * tile);
+    int best_chunk = std::max(gran, (p.cw + gran - 1) / gran * gran);
     for (int s = 1; s <= max_splits; ++s) {
         int chunk = (p.cw + s - 1) / s;
-        chunk = std::max(tile, (chunk + tile - 1) / tile * tile);
+        chunk = std::max(gran, (chunk + gran - 1) / gran * gran);
         const int s_eff = std::max(1, (p.cw + chunk - 1) / chunk);
         if (s_eff > split_cap)
             continue;
@@ -90,8 +92,14 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
         if (resident <= 0)
             continue;
         const long long waves = (units + resident - 1) / resident;
-        const double merge = s_eff > 1 ? (tc ? 0.5 : 1.0) : 0.0;
-        const double cost = (double)waves * ((double)chunk / tile + merge);
+        double per_worker;
+        if (tc) {
+            const int blocks = (chunk + tile - 1) / tile;
+            per_worker = blocks + 0.25 * chunk / tile + 0.5 + (s_eff > 1 ? 0.5 : 0.0);
+        } else {
+            per_worker = (double)chunk / tile + (s_eff > 1 ? 1.0 : 0.0);
+        }
+        const double cost = (double)waves * per_worker;
         if (cost < best - 1e-9) {
             best = cost;
             best_chunk = chunk;
@@ -279,15 +287,27 @@ extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_
     p.splits = pl.splits;
     p.chunk = pl.chunk;
     p.status = status;
+    p.topk = topk_idx;
+    p.topk_stride = topk_stride;
+    p.topk_width = topk_width;
+    p.topk_lens = topk_lens;
+    p.seq_lens = seq_lens;
+    p.window = window;
+    p.table_bits = pl.combine_table_bits;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_combine(topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens, window,
-                                   reinterpret_cast<int32_t *>(ws + pl.off_combined), pl.cw, pl.cw,
-                                   reinterpret_cast<int32_t *>(ws + pl.off_lens), pl.combine_table_bits, s);
-    if (e == cudaSuccess)
-        e = pl.path == kPathTc ? launch_decode_tc(p, s) : launch_decode_simt(p, s);
-    if (e == cudaSuccess && pl.path == kPathSimt)   // the tensor-core kernel merges its own splits
-        e = launch_merge(p, s);
+    cudaError_t e;
+    if (pl.path == kPathTc) {   // one launch: the kernel combines, decodes and merges its splits
+        e = launch_decode_tc(p, s);
+    } else {
+        e = launch_combine(topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens, window,
+                           reinterpret_cast<int32_t *>(ws + pl.off_combined), pl.cw, pl.cw,
+                           reinterpret_cast<int32_t *>(ws + pl.off_lens), pl.combine_table_bits, s);
+        if (e == cudaSuccess)
+            e = launch_decode_simt(p, s);
+        if (e == cudaSuccess)
+            e = launch_merge(p, s);
+    }
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 

@@ -1,41 +1,48 @@
-// decode_tc.cu -- tensor-core (tcgen05 / TMEM) sparse-MLA decode, 64 heads per CTA.
+// decode_tc.cu -- tensor-core (tcgen05 / TMEM) sparse-MLA decode, 64 heads per CTA, with the
+// top-k + sliding-window index combine fused into its prologue.
 //
 // Operation (per token t, head h, over the token's combined key list K_t):
 //   s_p = scale * q_h . k_p  (576 dims),  out_h = sum_p softmax(s)_p v_p  (512 dims)
-// with the gather/dequant of "feat: add DeepSeek-V4 XPU attention decode path"
-// (vllm #42953, _dequant_gather_slots_kernel: value = e4m3 * 2^(ue8m0 - 127), rope
-// as stored) and the per-request block-table conversion and [T, h, 512] output of
-// "Enable DeepSeek V4 and GLM-5.1 on SM120" (vllm #43477, flashinfer_mla_sparse_sm120.py).
+// with the combine of "[ROCm] [DSv4] [Perf] Support DeepSeek v4 MTP" (vllm #43385,
+// _combine_topk_swa_indices_kernel: kept top-k entries in input order, then the window
+// ascending), the gather/dequant of "feat: add DeepSeek-V4 XPU attention decode path"
+// (vllm #42953, _dequant_gather_slots_kernel: value = e4m3 * 2^(ue8m0 - 127), rope as
+// stored) and the per-request block-table conversion and [T, h, 512] output of "Enable
+// DeepSeek V4 and GLM-5.1 on SM120" (vllm #43477, flashinfer_mla_sparse_sm120.py).
 //
-// Shape of the contraction.  All heads share one key set (MQA), so a token is a
-// pair of dense products: S = Q K^T (64 x 576 x keys) and O = P V (64 x keys x 512).
-// With 64 heads the head dimension is too short to fill a 128-row tcgen05 tile, so
-// both products run transposed, keys and value dims on the M side:
+// Shape of the contraction.  All heads share one key set (MQA), so a token is a pair of
+// dense products: S = Q K^T (64 x 576 x keys) and O = P V (64 x keys x 512).  With 64
+// heads the head dimension is too short to fill a 128-row tcgen05 tile, so both products
+// run transposed, keys and value dims on the M side:
 //   S^T[128 keys x 64 heads]   = K_tile[128 x 576] . Q^T          (A = K tile, K-major)
 //   O^T[128 dv x 64 heads] += V^T[128 dv x 128 keys] . P^T        (A = K tile, MN-major)
-// One BF16 K tile in shared memory (128-byte swizzle, 8-row atoms, 64-dim column
-// chunks) is read by both: as K-major A for S^T (rows = keys) and, without any
-// copy, as MN-major A for O^T (rows of the same atoms = keys along K, the 64
-// contiguous dims along M).  S^T, O^T (four 128-dv tiles) and per-lane partial row
-// sums live in TMEM (512 columns).
+// One BF16 K tile in shared memory (128-byte swizzle, 8-row atoms, nine 64-dim column
+// chunks) is read by both: as K-major A for S^T and, without a copy, as MN-major A for O^T.
+// S^T, O^T (four 128-dv tiles) and per-lane partial row sums live in TMEM (512 columns).
 //
-// CTA = 512 threads, one (token, 64-head group, split):
-//   warp 0       tcgen05.alloc/dealloc; lane 0 issues the MMAs and commits
-//   warps 1-15   workers: 16-byte streaming loads of the next block's entries into
-//                registers while the current block computes, then the exact dequant
-//                (E4M3 -> f16 -> f32 * 2^(e-127) -> BF16) into the swizzled K tile;
-//                warps 1-3 also look up cache slots two blocks ahead
-//   warps 4-11   also the softmax: lane i of a warp owns TMEM lane i of its quadrant
-//                (key i of the block in S^T, a value dim in O^T), two warps per
-//                quadrant split the 64 heads; per-head block maxima with
-//                redux.sync.max.f32, lazy rescaling (only when a head's max grows by
-//                more than 2^8), P^T (BF16) into shared memory, row sums in TMEM
+// CTA = 16 warps, one (token, 64-head group, split).  Prologue: the CTA combines its
+// token's top-k row with the window (shared-memory hash set for first occurrences, block
+// scan for the output order), keeps the entries of its own split and resolves them through
+// the block table to cache slots: blocks 0 and 1 straight into shared memory, later blocks
+// into the workspace.  Per 128-key block:
+//   dequant   thread (row = tid / 4, quarter = tid % 4) holds its row's 16-byte pieces
+//             of the block in registers (loaded during the previous block) and writes the
+//             exact BF16 values chunk by chunk; chunk c of block b+1 is written as soon as
+//             the P.V product of block b has released it
+//   S^T       lane 0 of warp 0 issues the 4 MMAs of chunk c once every warp has written it,
+//             so the product trails the dequant by one chunk
+//   softmax   all 16 warps: warp w reads TMEM lanes 32 (w % 4).. (its keys) for heads
+//             16 (w / 4)..; per-head block maxima with redux.sync, lazy rescaling (only when
+//             a head's max grows by more than 2^8), P^T (BF16) into shared memory, row sums
+//             in TMEM
+//   O^T       32 MMAs, committed per 128-dv tile so the next block's dequant can start
 // When a token's keys are split over S CTAs (S <= 8), the S CTAs form a thread-block
 // cluster: each stages its partial in its own shared memory and, after a cluster
-// barrier, every CTA merges a slice of the heads by reading its peers' partials
-// through distributed shared memory.
-// Every mbarrier wait is bounded; a wait that runs out records DSV4_ERR_TIMEOUT in
-// the status word and the CTA finishes without waiting again.
+// barrier, every CTA merges a slice of the heads by reading its peers' partials through
+// distributed shared memory.
+// Every mbarrier wait is bounded; a wait that runs out records DSV4_ERR_TIMEOUT in the
+// status word and the CTA finishes without waiting again.
+#include <climits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -46,7 +53,8 @@
 namespace dsv4 {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 544;             // warp 0: MMA issue; warps 1-16: workers
+constexpr int kWorkers = 512;
 constexpr int kBK = 128;                 // keys per block = MMA M
 constexpr int kNH = 64;                  // heads per CTA = MMA N
 constexpr int kChunks = 9;               // 576 dims / 64
@@ -54,12 +62,8 @@ constexpr int kQBytes = kChunks * kNH * 128;     // 73728
 constexpr int kKBytes = kChunks * kBK * 128;     // 147456
 constexpr int kChunkBytes = kBK * 128;           // 16384 (one 64-dim column chunk of the K tile)
 constexpr int kQChunkBytes = kNH * 128;          // 8192
-constexpr int kWorkers = 480;                    // warps 1-15: loads + dequant (and softmax on warps 4-11)
-constexpr int kDataPieces = 40;                  // 16-byte pieces per entry holding data (32 latent + 8 rope)
-constexpr int kRowGroups = kWorkers / kDataPieces;     // 12: worker w owns piece w % 40 of rows w / 40 + 12 i
-constexpr int kRowsPerLoader = (kBK + kRowGroups - 1) / kRowGroups;   // 11
-constexpr int kSoftWarps = 8;            // two per TMEM lane quadrant, 32 heads each
-constexpr int kSoftThreads = 32 * kSoftWarps;
+constexpr int kHeadSlots = 2 * kBK;      // cache slots of blocks 0 and 1, found in the prologue
+constexpr int kPassLoads = 4;            // combine: top-k entries per thread loaded up front
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;            // S^T: 64 columns
 constexpr uint32_t kColO = 64;           // O^T: 4 tiles x 64 columns
@@ -69,19 +73,23 @@ constexpr long long kWaitCycles = 4000000000LL;
 constexpr int kMaxSplits = 8;            // portable cluster size
 
 // small shared region (after Q and the K tile)
-constexpr int kOffSlots = 0;             // int [3][128]
-constexpr int kOffScale = 1536;          // uint [128]
-constexpr int kOffRed = 2048;            // float [4][64]
-constexpr int kOffMrun = 3072;           // float [64]
-constexpr int kOffMc = 3328;             // float [64]
-constexpr int kOffAlpha = 3584;          // float [64]
-constexpr int kOffFin = 3840;            // float [64]
-constexpr int kOffBars = 4096;           // u64 [3]
-constexpr int kOffTmem = 4128;           // u32
-constexpr int kOffFlags = 4136;          // int [2]
-constexpr int kSmallBytes = 4160;
+constexpr int kOffSlots = 0;             // int [3][128]: cache slots of blocks b, b+1, b+2
+constexpr int kOffRed = 1536;            // float [4][64]
+constexpr int kOffMrun = 2560;           // float [64]
+constexpr int kOffMc = 2816;             // float [64]
+constexpr int kOffAlpha = 3072;          // float [64]
+constexpr int kOffFin = 3328;            // float [64]
+constexpr int kOffWsum = 3584;           // int [32]
+constexpr int kOffBars = 3712;           // u64: bar_s, bar_p, bar_pv[4], bar_grp[3]
+constexpr int kOffTmem = 3784;           // u32
+constexpr int kOffFlags = 3792;          // int [2]
+constexpr int kSmallBytes = 3840;
 constexpr int kSmemBytes = kQBytes + kKBytes + kSmallBytes + 1024;   // + alignment slack
-constexpr int kQLoads = kNH * (kDim / 8) / kThreads;                 // 9 16-byte Q pieces per thread
+constexpr int kQLoads = kNH * (kDim / 8) / kWorkers;                 // 9 16-byte Q pieces per worker
+constexpr int kGroups = 3;               // S^T is issued in 3 groups of 3 column chunks
+static_assert(kNH * (kDim / 8) % kWorkers == 0, "Q pieces per worker");
+static_assert(kKBytes >= 2 * (int)sizeof(int) * 2 * kMaxTopkWidth, "combine hash table fits the K tile");
+static_assert(kKBytes >= kNH * kLatent * (int)sizeof(float), "partial O fits the K tile");
 
 // instruction descriptors (kind::f16): D f32, A/B bf16, M = 128, N = 64
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kNH >> 3) << 17) |
@@ -133,8 +141,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 
 // Bounded wait on one phase of an mbarrier by a single thread.  After any timeout in
 // the CTA (abort flag set) waits return at once, so the CTA still reaches its end.
-__device__ __forceinline__ void mbar_wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                              unsigned *status)
+__device__ __noinline__ void mbar_wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *status)
 {
     if (*abort_flag)
         return;
@@ -180,18 +187,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-                 : "r"(taddr));
-}
-
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -201,12 +196,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
                  : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
 {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                 "%16};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                  : "memory");
 }
 
@@ -243,7 +243,8 @@ __device__ __forceinline__ float ue8m0_to_float(unsigned e)
     return __int_as_float((int)(e << 23));
 }
 
-// two E4M3 codes (low byte = first element) -> BF16x2 of code * scale (exact for in-range values)
+// two E4M3 codes (low byte = first element) -> BF16x2 of code * scale through the hardware
+// conversion (exact for every code and scale)
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float scale)
 {
     const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
@@ -251,6 +252,52 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float scale)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y * scale), "f"(f.x * scale));
     return r;
+}
+
+// The hardware-conversion form of dequant16_store below, kept out of line: it only runs
+// for pieces holding the NaN code or a scale past 2^7.
+__device__ __noinline__ void dequant16_store_convert(uint4 v, uint32_t se, uint32_t a0, uint32_t a1)
+{
+    const float sc = ue8m0_to_float(se);
+    st_shared_v4(a0, e4m3x2_to_bf16x2(v.x, sc), e4m3x2_to_bf16x2(v.x >> 16, sc), e4m3x2_to_bf16x2(v.y, sc),
+                 e4m3x2_to_bf16x2(v.y >> 16, sc));
+    st_shared_v4(a1, e4m3x2_to_bf16x2(v.z, sc), e4m3x2_to_bf16x2(v.z >> 16, sc), e4m3x2_to_bf16x2(v.w, sc),
+                 e4m3x2_to_bf16x2(v.w >> 16, sc));
+}
+
+// 16 E4M3 codes times 2^(se - 127) -> 16 BF16, elements 0-7 to shared address a0 and 8-15 to a1.
+// An E4M3 code s.eeee.mmm placed as the BF16 pattern s.0000eeee.mmm0000 is its value times
+// 2^-120 for normal and subnormal codes alike (both formats put the binary point the same
+// way; only the exponent biases, 7 and 127, differ).  One BF16 multiply by 2^(se - 7) then
+// gives the value exactly rounded.  The NaN code (magnitude 0x7F) and scales past 2^7
+// (se > 134, whose factor has no BF16 form) take the hardware conversion instead.
+__device__ __forceinline__ void dequant16_store(uint4 v, uint32_t se, uint32_t a0, uint32_t a1)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t t[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        t[2 * i] = __byte_perm(w[i], 0u, 0x1404);       // [0, c0, 0, c1]
+        t[2 * i + 1] = __byte_perm(w[i], 0u, 0x3424);   // [0, c2, 0, c3]
+    }
+    uint32_t bad = se > 134u ? 1u : 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        bad |= ((t[i] & 0x7F007F00u) + 0x01000100u) & 0x80008000u;   // magnitude 0x7F present
+    if (bad == 0u) {
+        uint32_t f = (se + 120u) << 7;
+        f |= f << 16;
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t x = (t[i] & 0x80008000u) | ((t[i] & 0x7F007F00u) >> 4);
+            asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(x), "r"(f));
+        }
+        st_shared_v4(a0, o[0], o[1], o[2], o[3]);
+        st_shared_v4(a1, o[4], o[5], o[6], o[7]);
+    } else {
+        dequant16_store_convert(v, se, a0, a1);
+    }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -265,8 +312,6 @@ __device__ __forceinline__ uint16_t bf16_bits(float v)
     const __nv_bfloat16 b = __float2bfloat16_rn(v);
     return *reinterpret_cast<const uint16_t *>(&b);
 }
-
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---- thread-block cluster: the splits of one (token, head group) merge over distributed shared memory
 __device__ __forceinline__ void cluster_sync()
@@ -302,49 +347,52 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr)
 // Every CTA has staged, in its own shared memory, its running max m_s (natural-log
 // units, s_m[h]) and row sum l_s (s_l[h]) per head and its unnormalised O_s as fp32
 // [64 heads][512] (s_o).  After a cluster barrier the CTA of rank r merges heads
-// [r*hp, (r+1)*hp) (hp = ceil(64 / S)), reading all S partials through distributed
-// shared memory with the loads of all splits in flight together:
+// [r*hp, (r+1)*hp) (hp = ceil(64 / S)):
 //   m = max(max_s m_s, sink), Z = sum_s l_s e^{m_s - m} + e^{sink - m},
 //   out = sum_s e^{m_s - m} O_s / Z  (BF16),  lse = m + ln Z.
-__device__ void cluster_merge_pull(const DecodeParams &p, int t, int h0, int rank, uint32_t s_m, uint32_t s_l,
-                                   uint32_t s_o, float *wts)
+// The statistics of all (head, split) pairs are pulled at once, one per thread; the O rows
+// are pulled two 16-byte pieces per thread at a time with the loads of all splits in flight.
+__device__ __noinline__ void cluster_merge_pull(uint16_t *out, float *lse, const float *sink, int num_heads, int S,
+                                                int t, int h0, int rank, uint32_t s_m, uint32_t s_l, uint32_t s_o,
+                                                float *scratch)
 {
-    const int S = p.splits;
     const int hp = (kNH + S - 1) / S;
     const int hb = rank * hp;
-    const int he = min(kNH, hb + hp);
+    const int nh = max(0, min(kNH, hb + hp) - hb);
     const int tid = threadIdx.x;
-    if (tid < he - hb) {
+    float *pm = scratch;            // [64][8] pulled maxima
+    float *pl = scratch + 512;      // [64][8] pulled row sums
+    float *wts = scratch + 1024;    // [64][10]: weight per split (divided by Z), then the lse
+    if (tid < nh * S) {
+        const int hl = tid / S;
+        const int s = tid % S;
+        pm[hl * 8 + s] = ld_cluster_f32(map_to_rank(s_m + 4u * (hb + hl), s));
+        pl[hl * 8 + s] = ld_cluster_f32(map_to_rank(s_l + 4u * (hb + hl), s));
+    }
+    __syncthreads();
+    if (tid < nh) {
         const int h = hb + tid;
-        float ms[kMaxSplits], ls[kMaxSplits];
-#pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s) {
-            ms[s] = s < S ? ld_cluster_f32(map_to_rank(s_m + 4u * h, s)) : -INFINITY;
-            ls[s] = s < S ? ld_cluster_f32(map_to_rank(s_l + 4u * h, s)) : 0.f;
-        }
         float m = -INFINITY;
-#pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s)
-            m = fmaxf(m, ms[s]);
+        for (int s = 0; s < S; ++s)
+            m = fmaxf(m, pm[tid * 8 + s]);
         const float mk = m;
         float sk = 0.f;
-        if (p.sink != nullptr) {
-            sk = p.sink[h0 + h];
+        if (sink != nullptr) {
+            sk = sink[h0 + h];
             m = fmaxf(m, sk);
         }
         float z = 0.f;
-        float w[kMaxSplits];
-#pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s) {
-            w[s] = ms[s] == -INFINITY ? 0.f : expf(ms[s] - m);
-            z += ls[s] * w[s];
+        for (int s = 0; s < S; ++s) {
+            const float ms = pm[tid * 8 + s];
+            const float w = ms == -INFINITY ? 0.f : expf(ms - m);
+            wts[tid * 10 + s] = w;
+            z += pl[tid * 8 + s] * w;
         }
-        if (p.sink != nullptr)
+        if (sink != nullptr)
             z += expf(sk - m);
         const float f = (z > 0.f && mk != -INFINITY) ? 1.f / z : 0.f;
-#pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s)
-            wts[tid * 10 + s] = w[s] * f;
+        for (int s = 0; s < S; ++s)
+            wts[tid * 10 + s] *= f;
         wts[tid * 10 + 8] = z > 0.f ? m + logf(z) : -INFINITY;
     }
     __syncthreads();
@@ -352,44 +400,54 @@ __device__ void cluster_merge_pull(const DecodeParams &p, int t, int h0, int ran
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s)
         peer[s] = s < S ? map_to_rank(s_o, s) : 0u;
-    for (int i = tid; i < (he - hb) * (kLatent / 4); i += kThreads) {
-        const int hl = i / (kLatent / 4);
-        const int c = i % (kLatent / 4);
-        const uint32_t off = (uint32_t)((hb + hl) * kLatent + 4 * c) * 4u;
-        float4 v[kMaxSplits];
+    const int items = nh * (kLatent / 4);   // 16-byte pieces of the slice
+    for (int i = tid; i < items; i += 2 * kThreads) {
+        float4 v[2][kMaxSplits];
+        int hl[2], c[2];
+        bool ok[2];
 #pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s)
-            v[s] = (s < S && wts[hl * 10 + s] != 0.f) ? ld_cluster_v4(peer[s] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < 2; ++u) {
+            const int iu = i + u * kThreads;
+            ok[u] = iu < items;
+            hl[u] = ok[u] ? iu / (kLatent / 4) : 0;
+            c[u] = iu % (kLatent / 4);
+            const uint32_t off = (uint32_t)((hb + hl[u]) * kLatent + 4 * c[u]) * 4u;
 #pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s) {
-            const float ws = wts[hl * 10 + s];
-            acc.x = fmaf(ws, v[s].x, acc.x);
-            acc.y = fmaf(ws, v[s].y, acc.y);
-            acc.z = fmaf(ws, v[s].z, acc.z);
-            acc.w = fmaf(ws, v[s].w, acc.w);
+            for (int s = 0; s < kMaxSplits; ++s)
+                v[u][s] = (ok[u] && s < S && wts[hl[u] * 10 + s] != 0.f) ? ld_cluster_v4(peer[s] + off)
+                                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        uint2 u;
-        u.x = pack_bf16x2(acc.x, acc.y);
-        u.y = pack_bf16x2(acc.z, acc.w);
-        const int h = h0 + hb + hl;
-        *reinterpret_cast<uint2 *>(p.out + ((int64_t)t * p.num_heads + h) * kLatent + 4 * c) = u;
-        if (c == 0 && p.lse != nullptr)
-            p.lse[(int64_t)t * p.num_heads + h] = wts[hl * 10 + 8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!ok[u])
+                continue;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int s = 0; s < kMaxSplits; ++s) {
+                const float ws = s < S ? wts[hl[u] * 10 + s] : 0.f;
+                acc.x = fmaf(ws, v[u][s].x, acc.x);
+                acc.y = fmaf(ws, v[u][s].y, acc.y);
+                acc.z = fmaf(ws, v[u][s].z, acc.z);
+                acc.w = fmaf(ws, v[u][s].w, acc.w);
+            }
+            uint2 o;
+            o.x = pack_bf16x2(acc.x, acc.y);
+            o.y = pack_bf16x2(acc.z, acc.w);
+            const int h = h0 + hb + hl[u];
+            *reinterpret_cast<uint2 *>(out + ((int64_t)t * num_heads + h) * kLatent + 4 * c[u]) = o;
+            if (c[u] == 0 && lse != nullptr)
+                lse[(int64_t)t * num_heads + h] = wts[hl[u] * 10 + 8];
+        }
     }
 }
 
-// Logical position of key `k` of block `b` -> cache slot (phys_block * page + offset), or -1.
-__device__ __forceinline__ int slot_of(const DecodeParams &p, int t, int row, bool row_ok, int kbeg, int kend, int b,
-                                       int k)
+// Logical position -> cache slot (phys_block * page + offset) through the token's
+// block-table row; -1 (and the bad-index status bit) when the table has no valid block.
+__device__ __forceinline__ int slot_of_position(const DecodeParams &p, int row, int idx)
 {
-    const int i = kbeg + b * kBK + k;
-    if (i >= kend || !row_ok)
-        return -1;
-    const int idx = p.combined[(int64_t)t * p.cw + i];
-    const int blk = idx >= 0 ? idx / p.page : -1;
+    const int blk = idx / p.page;
     int phys = -1;
-    if (idx >= 0 && blk < p.max_blocks)
+    if (blk < p.max_blocks)
         phys = p.block_table[(int64_t)row * p.bt_stride + blk];
     if (phys < 0 || phys >= p.num_blocks) {
         atomicOr(p.status, kStatusBadIndex);
@@ -397,6 +455,8 @@ __device__ __forceinline__ int slot_of(const DecodeParams &p, int t, int row, bo
     }
     return phys * p.page + (idx - blk * p.page);
 }
+
+__device__ __forceinline__ unsigned hash_pos(int v, int bits) { return ((unsigned)v * 0x9E3779B1u) >> (32 - bits); }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeParams p)
 {
@@ -409,17 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int group = (unit / p.splits) % p.groups;
     const int t = unit / (p.splits * p.groups);
     const int h0 = group * kNH;
+    const bool is_mma = warp == 0;
+    const int wid = tid - 32;            // worker index 0..511 (warps 1-16)
 
-    // Q does not depend on the combine kernel: its loads go out before waiting for it
-    uint4 qv[kQLoads];
-#pragma unroll
-    for (int j = 0; j < kQLoads; ++j) {
-        const int i = tid + kThreads * j;
-        const int h = i / (kDim / 8);
-        const int c = i % (kDim / 8);
-        qv[j] = __ldg(reinterpret_cast<const uint4 *>(p.q + (int64_t)t * p.q_token_stride + (int64_t)(h0 + h) * kDim +
-                                                       8 * c));
-    }
+    // every input may come from the previous kernel in the stream; the next kernel may be
+    // scheduled now (it waits for this grid's results itself)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- shared memory carve-up (1024-byte aligned base for the swizzled tiles)
     const uint32_t raw = smem_u32(smem_raw);
@@ -430,32 +486,140 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const uint32_t sP = sK + 8 * kChunkBytes;   // P^T reuses the rope column chunk once S^T is done
     uint8_t *small = gbase + kQBytes + kKBytes;
     int *slots = reinterpret_cast<int *>(small + kOffSlots);
-    unsigned *scal = reinterpret_cast<unsigned *>(small + kOffScale);
     float *red = reinterpret_cast<float *>(small + kOffRed);
     float *mrun = reinterpret_cast<float *>(small + kOffMrun);
     float *mcs = reinterpret_cast<float *>(small + kOffMc);
     float *alpha = reinterpret_cast<float *>(small + kOffAlpha);   // at the end: this split's max per head
     float *fin = reinterpret_cast<float *>(small + kOffFin);       // at the end: this split's row sum per head
-    const uint32_t bar_s = smem_u32(small + kOffBars);
-    const uint32_t bar_p = bar_s + 8;
-    const uint32_t bar_o = bar_s + 16;
+    int *wsum = reinterpret_cast<int *>(small + kOffWsum);
+    const uint32_t bar_s = smem_u32(small + kOffBars);   // S^T of the block complete
+    const uint32_t bar_p = bar_s + 8;                    // P^T and row sums of the block written (16 warps)
+    const uint32_t bar_pv = bar_s + 16;                  // [4] O^T tiles 0..m of the block complete
+    const uint32_t bar_grp = bar_s + 48;                 // [3] column chunks 3g..3g+2 of the K tile written
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small + kOffTmem);
     volatile int *flags = reinterpret_cast<volatile int *>(small + kOffFlags);   // [0] abort, [1] rescale block tag
-    float *wts = reinterpret_cast<float *>(gbase + 40960);   // merge weights (Q region, idle at the end)
     float *o_stage = reinterpret_cast<float *>(gbase + kQBytes);   // partial O [64][512] fp32 (K tile region)
+    int *hkey = reinterpret_cast<int *>(gbase + kQBytes);          // combine hash set (K tile region)
 
-    grid_dependency_wait();   // combined lists and lengths are ready
-
-    const int L = p.lens[t];
-    const int kbeg = split * p.chunk;
-    const int kend = min(L, kbeg + p.chunk);
-    const int nkeys = max(0, kend - kbeg);
-    const int nblocks = (nkeys + kBK - 1) / kBK;
+    // ---- early loads: the token's sizes and top-k run first (the combine waits on them), then Q
+    const int seq_len = p.seq_lens[t];
+    const int W = p.topk_width;
+    int n = W;
+    if (p.topk_lens != nullptr) {
+        n = p.topk_lens[t];
+        n = n < 0 ? 0 : (n > W ? W : n);
+    }
     const int row = p.req_idx ? p.req_idx[t] : t;
     const bool row_ok = row >= 0 && row < p.num_reqs;
-    const float c2 = p.scale * 1.4426950408889634f;   // logits in log2 units per raw dot product
+    const int32_t *trow = p.topk + (int64_t)t * p.topk_stride;
+    const int npass = (n + kThreads - 1) / kThreads;   // the combine visits entry pass * kThreads + tid
+    int tv[kPassLoads];
+#pragma unroll
+    for (int u = 0; u < kPassLoads; ++u)
+        tv[u] = u < npass && u * kThreads + tid < n ? __ldg(trow + u * kThreads + tid) : -1;
+    uint4 qv[kQLoads];
+    if (!is_mma) {
+#pragma unroll
+        for (int j = 0; j < kQLoads; ++j) {
+            const int i = wid + kWorkers * j;
+            const int h = i / (kDim / 8);
+            const int c = i % (kDim / 8);
+            qv[j] = __ldg(reinterpret_cast<const uint4 *>(p.q + (int64_t)t * p.q_token_stride +
+                                                           (int64_t)(h0 + h) * kDim + 8 * c));
+        }
+    }
+
+    // ---- fused combine (kept top-k entries in input order, then the window ascending):
+    // window [win_lo, pos]; the top-k survivors are the first occurrences of positions in [0, win_lo)
+    const int pos = seq_len - 1;   // seq_len <= 0: nothing is visible
+    const long long lo = (long long)pos - p.window + 1;
+    const int win_lo = lo < 0 ? 0 : (int)lo;
+    const int swa = seq_len > 0 ? pos - win_lo + 1 : 0;
+    const int bits = p.table_bits;
+    const int table = 1 << bits;
+    int *hmin = hkey + table;
+    for (int i = tid; i < table; i += kThreads) {
+        hkey[i] = -1;
+        hmin[i] = INT_MAX;
+    }
+    if (tid < kHeadSlots)
+        slots[tid] = -1;
+    __syncthreads();
+    // first occurrence of each position: the smallest top-k index holding it
+    auto insert = [&](int v, int i) {
+        unsigned h = hash_pos(v, bits);
+        while (true) {
+            const int prev = atomicCAS(&hkey[h], -1, v);
+            if (prev == -1 || prev == v) {
+                atomicMin(&hmin[h], i);
+                return;
+            }
+            h = (h + 1u) & (unsigned)(table - 1);
+        }
+    };
+#pragma unroll
+    for (int u = 0; u < kPassLoads; ++u)
+        if (tv[u] >= 0 && tv[u] < win_lo)
+            insert(tv[u], u * kThreads + tid);
+#pragma unroll 1
+    for (int ps = kPassLoads; ps < npass; ++ps) {
+        const int i = ps * kThreads + tid;
+        const int v = i < n ? __ldg(trow + i) : -1;
+        if (v >= 0 && v < win_lo)
+            insert(v, i);
+    }
+    __syncthreads();
+    // survivors in input order: a ballot scan per pass; the ones of this split resolve to cache slots
+    const int kbeg = split * p.chunk;
+    const int klim = kbeg + p.chunk;
+    int32_t *slot_row = p.combined + (int64_t)t * p.cw;   // cache slots of blocks >= 2 of this split
+    int total = 0;
+#pragma unroll 1
+    for (int ps = 0; ps < npass; ++ps) {
+        const int i = ps * kThreads + tid;
+        const int v = i < n ? __ldg(trow + i) : -1;   // cached by the first pass
+        bool keep = false;
+        if (v >= 0 && v < win_lo) {
+            unsigned h = hash_pos(v, bits);
+            while (hkey[h] != v)
+                h = (h + 1u) & (unsigned)(table - 1);
+            keep = hmin[h] == i;
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (lane == 0)
+            wsum[warp] = __popc(bal);
+        __syncthreads();
+        int rank = total + __popc(bal & ((1u << lane) - 1u));
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            rank += w < warp ? wsum[w] : 0;
+            total += wsum[w];
+        }
+        if (keep && row_ok && rank >= kbeg && rank < klim) {
+            const int sl = slot_of_position(p, row, v);
+            if (rank - kbeg < kHeadSlots)
+                slots[rank - kbeg] = sl;
+            else
+                slot_row[rank] = sl;
+        }
+        __syncthreads();   // wsum is rewritten by the next pass
+    }
+
+    const int L = total + swa;
+    const int kend = min(L, klim);
+    const int nkeys = max(0, kend - kbeg);
+    const int nblocks = (nkeys + kBK - 1) / kBK;
     if (!row_ok && tid == 0 && nkeys > 0)
         atomicOr(p.status, kStatusBadIndex);
+    if (row_ok) {   // the window part of this split
+        for (int i = max(kbeg, total) + tid; i < kend; i += kThreads) {
+            const int sl = slot_of_position(p, row, win_lo + (i - total));
+            if (i - kbeg < kHeadSlots)
+                slots[i - kbeg] = sl;
+            else
+                slot_row[i] = sl;
+        }
+    }
 
     if (nblocks == 0) {   // no key in this split
         if (p.splits == 1) {   // zero output, LSE from the sink alone
@@ -474,23 +638,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             fin[tid] = 0.f;
         }
         cluster_sync();   // every split has staged its partial
-        cluster_merge_pull(p, t, h0, split, smem_u32(alpha), smem_u32(fin), sK, wts);
+        cluster_merge_pull(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split, smem_u32(alpha), smem_u32(fin),
+                           sK, reinterpret_cast<float *>(gbase));
         cluster_sync();   // peers have finished reading this CTA's shared memory
         return;
     }
 
-    const bool is_mma = warp == 0;
-    const bool is_soft = warp >= 4 && warp < 4 + kSoftWarps;
-    const int wk = tid - 32;                              // worker index 0..479 (warps 1-15)
-    const int stid = tid - 128;                           // softmax thread index 0..255 (warps 4-11)
     const int quad = warp & 3;                            // TMEM lane quadrant of this warp
-    const int hh = (warp - 4) >> 2;                       // softmax: head half (heads 32 hh .. 32 hh + 31)
+    const int hs = 16 * ((warp - 1) >> 2);                // workers: first of this warp's 16 heads
     const int key = quad * 32 + lane;                     // softmax: key of the block / value dim of a tile
+    // dequant: lane l of worker warp ww takes quarter l % 4 of row 8 ((ww - l / 4) mod 16) + l / 4, so a
+    // warp's 8 rows differ in row % 8 (no bank conflicts in the swizzled stores) and the first rows of a
+    // block spread over all warps
+    const int qtr = lane & 3;
+    const int rrow = 8 * (((warp - 1) - (lane >> 2)) & 15) + (lane >> 2);
+    const float c2 = p.scale * 1.4426950408889634f;      // logits in log2 units per raw dot product
 
     if (tid == 0) {
         mbar_init(bar_s, 1);
-        mbar_init(bar_p, kSoftWarps);
-        mbar_init(bar_o, 1);
+        mbar_init(bar_p, kWorkers / 32);
+        for (int m = 0; m < 4; ++m)
+            mbar_init(bar_pv + 8 * m, 1);
+        for (int g = 0; g < kGroups; ++g)
+            mbar_init(bar_grp + 8 * g, kWorkers / 32);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         flags[0] = 0;
         flags[1] = 0;
@@ -502,21 +672,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                      "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    // cache slots of blocks 0 and 1, one lookup per thread
-    if (tid < 2 * kBK)
-        slots[tid] = slot_of(p, t, row, row_ok, kbeg, kend, tid / kBK, tid % kBK);
-    // Q (64 heads x 576 dims) -> swizzled K-major B operand
+    } else {   // Q -> swizzled K-major B operand
 #pragma unroll
-    for (int j = 0; j < kQLoads; ++j) {
-        const int i = tid + kThreads * j;
-        const int h = i / (kDim / 8);
-        const int c = i % (kDim / 8);
-        st_shared_v4(sQ + (c >> 3) * kQChunkBytes + sw128(h, c & 7), qv[j].x, qv[j].y, qv[j].z, qv[j].w);
+        for (int j = 0; j < kQLoads; ++j) {
+            const int i = wid + kWorkers * j;
+            const int h = i / (kDim / 8);
+            const int c = i % (kDim / 8);
+            st_shared_v4(sQ + (c >> 3) * kQChunkBytes + sw128(h, c & 7), qv[j].x, qv[j].y, qv[j].z, qv[j].w);
+        }
     }
     fence_async_smem();
     tc_before();
-    __syncthreads();
+    __syncthreads();   // slots of blocks 0/1, Q, barriers, TMEM address; the hash set is dead
     tc_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);   // this warp's TMEM lanes
@@ -530,125 +697,121 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         const uint64_t pv_b = sdesc(sP, 1024, 1024);   // one 64-head group along N: LBO unused, kept = SBO
         for (int b = 0; b < nblocks; ++b) {
             const uint32_t ph = (uint32_t)(b & 1);
-            named_bar(3, kThreads);   // K tile of block b complete
             if (lane == 0) {
-                tc_after();
 #pragma unroll
-                for (int ch = 0; ch < kChunks; ++ch) {
+                for (int g = 0; g < kGroups; ++g) {
+                    mbar_wait_one(bar_grp + 8 * g, ph, flags, p.status);   // chunks 3g..3g+2 written
+                    tc_after();
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        umma(tmem + kColS, qk_a + (uint64_t)((ch * kChunkBytes + 32 * k) >> 4),
-                             qk_b + (uint64_t)((ch * kQChunkBytes + 32 * k) >> 4), kIdescQK, (ch | k) != 0 ? 1u : 0u);
+                    for (int c = 3 * g; c < 3 * g + 3; ++c) {
+                        const uint64_t a = qk_a + (uint64_t)((c * kChunkBytes) >> 4);
+                        const uint64_t bq = qk_b + (uint64_t)((c * kQChunkBytes) >> 4);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            umma(tmem + kColS, a + (uint64_t)(2 * k), bq + (uint64_t)(2 * k), kIdescQK,
+                                 (c | k) != 0 ? 1u : 0u);
+                    }
                 }
                 umma_commit(bar_s);
-                mbar_wait_one(bar_p, ph, flags, p.status);
+                mbar_wait_one(bar_p, ph, flags, p.status);   // P^T of block b written
                 tc_after();
+                const int ksteps = min(kBK / 16, (nkeys - b * kBK + 15) / 16);   // 16-key steps holding keys
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
+                for (int m = 0; m < 4; ++m) {
+                    const uint64_t a = pv_a + (uint64_t)((2 * m * kChunkBytes) >> 4);
 #pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        umma(tmem + kColO + 64 * m, pv_a + (uint64_t)((2 * m * kChunkBytes + kk * 2048) >> 4),
-                             pv_b + (uint64_t)((kk * 2048) >> 4), kIdescPV, (b > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        if (kk < ksteps)
+                            umma(tmem + kColO + 64 * m, a + (uint64_t)(kk * 128), pv_b + (uint64_t)(kk * 128), kIdescPV,
+                             (b > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(bar_pv + 8 * m);   // releases K chunks 2m, 2m+1 (tile 3: also P^T)
                 }
-                umma_commit(bar_o);
             }
             __syncwarp();
         }
     } else {
-        // ---- workers.  Worker wk owns 16-byte piece pc = wk % 40 of rows rg, rg + 12, ... of every
-        // block (pieces 0-31 latent, 32-39 rope); workers 0-127 also fetch the scale word of row wk.
-        const int pc = wk % kDataPieces;
-        const int rg = wk / kDataPieces;
-        const bool latent = pc < 32;
-        const int chunk = latent ? pc >> 2 : 8;
-        const uint32_t u0 = latent ? (uint32_t)(pc & 3) * 2u : (uint32_t)(pc - 32);
-        const bool odd = latent && (chunk & 1);   // neighbouring chunks store their two units in opposite order
-        const int scale_shift = 8 * (pc >> 3);
-        uint4 pre[kRowsPerLoader];
-        unsigned pre_scale = 0;
+        // registers for the next block: 8 latent pieces, 2 rope pieces and the scale word of row rrow
+        uint4 pre[10];
+        uint32_t pre_sw = 0;
+        bool pre_ok = false;
         auto issue_loads = [&](int b) {
-            const int *sl = slots + (b % 3) * kBK;
+            const int sidx = slots[(b % 3) * kBK + rrow];
+            pre_ok = sidx >= 0;
+            if (pre_ok) {
+                const uint8_t *e = p.kv + (int64_t)sidx * kEntryBytes;
 #pragma unroll
-            for (int it = 0; it < kRowsPerLoader; ++it) {
-                const int r = rg + kRowGroups * it;
-                const int sidx = r < kBK ? sl[r] : -1;
-                pre[it] = sidx >= 0 ? ld_stream(p.kv + (int64_t)sidx * kEntryBytes + 16 * pc) : make_uint4(0, 0, 0, 0);
-            }
-            if (wk < kBK) {
-                const int sidx = sl[wk];
-                pre_scale = sidx >= 0 ? __ldg(reinterpret_cast<const unsigned *>(p.kv + (int64_t)sidx * kEntryBytes +
-                                                                                  kScaleOffset))
-                                      : 0u;
+                for (int c = 0; c < 8; ++c)
+                    pre[c] = ld_stream(e + 64 * c + 16 * qtr);
+                pre[8] = ld_stream(e + kRopeOffset + 16 * qtr);
+                pre[9] = ld_stream(e + kRopeOffset + 64 + 16 * qtr);
+                pre_sw = __ldg(reinterpret_cast<const unsigned *>(e + kScaleOffset));
             }
         };
         issue_loads(0);
+
         for (int b = 0; b < nblocks; ++b) {
             const uint32_t ph = (uint32_t)(b & 1);
-            if (b > 0)
-                mbar_wait(bar_o, ph ^ 1u, flags, p.status);   // P.V has drained the tile
-            if (wk < kBK)
-                scal[wk] = pre_scale;
-            named_bar(2, kWorkers);
-            // the row addresses are recomputed each block (an opaque copy of rg stops the compiler
-            // from hoisting 22 of them into registers for the whole loop)
-            int rgb = rg;
-            asm volatile("" : "+r"(rgb));
+            // ---- dequant of block b into the K tile, chunk by chunk (zeros for rows without a key)
+            {
+                const uint32_t rb = sK + (uint32_t)(rrow >> 3) * 1024u + (uint32_t)(rrow & 7) * 128u;
+                const uint32_t x7 = (uint32_t)(rrow & 7);
+                const uint32_t u0 = (((uint32_t)(2 * qtr)) ^ x7) << 4;
+                const uint32_t u1 = (((uint32_t)(2 * qtr + 1)) ^ x7) << 4;
 #pragma unroll
-            for (int it = 0; it < kRowsPerLoader; ++it) {
-                const int r = rgb + kRowGroups * it;
-                if (r >= kBK)
-                    continue;
-                const uint32_t rowbase = sK + (uint32_t)chunk * kChunkBytes + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
-                const uint4 v = pre[it];
-                if (latent) {
-                    const float sc = ue8m0_to_float((scal[r] >> scale_shift) & 0xFFu);
-                    const uint32_t a0 = e4m3x2_to_bf16x2(v.x, sc), a1 = e4m3x2_to_bf16x2(v.x >> 16, sc);
-                    const uint32_t a2 = e4m3x2_to_bf16x2(v.y, sc), a3 = e4m3x2_to_bf16x2(v.y >> 16, sc);
-                    const uint32_t b0 = e4m3x2_to_bf16x2(v.z, sc), b1 = e4m3x2_to_bf16x2(v.z >> 16, sc);
-                    const uint32_t b2 = e4m3x2_to_bf16x2(v.w, sc), b3 = e4m3x2_to_bf16x2(v.w >> 16, sc);
-                    const uint32_t uf = u0 + (odd ? 1u : 0u);
-                    const uint32_t us = u0 + (odd ? 0u : 1u);
-                    st_shared_v4(rowbase + ((uf ^ (uint32_t)(r & 7)) << 4), odd ? b0 : a0, odd ? b1 : a1,
-                                 odd ? b2 : a2, odd ? b3 : a3);
-                    st_shared_v4(rowbase + ((us ^ (uint32_t)(r & 7)) << 4), odd ? a0 : b0, odd ? a1 : b1,
-                                 odd ? a2 : b2, odd ? a3 : b3);
-                } else {
-                    st_shared_v4(rowbase + ((u0 ^ (uint32_t)(r & 7)) << 4), v.x, v.y, v.z, v.w);
+                for (int c = 0; c < kChunks; ++c) {
+                    if (b > 0 && c < 8 && (c & 1) == 0)
+                        mbar_wait(bar_pv + 8 * (c >> 1), ph ^ 1u, flags, p.status);   // P.V of block b-1 released it
+                    const uint32_t cb = rb + (uint32_t)c * kChunkBytes;
+                    if (!pre_ok) {
+                        const uint32_t ua = c < 8 ? u0 : ((((uint32_t)qtr) ^ x7) << 4);
+                        const uint32_t ub = c < 8 ? u1 : ((((uint32_t)qtr + 4u) ^ x7) << 4);
+                        st_shared_v4(cb + ua, 0u, 0u, 0u, 0u);
+                        st_shared_v4(cb + ub, 0u, 0u, 0u, 0u);
+                    } else if (c < 8) {
+                        dequant16_store(pre[c], (pre_sw >> (8 * (c >> 1))) & 0xFFu, cb + u0, cb + u1);
+                    } else {   // rope units qtr and qtr + 4, as stored
+                        st_shared_v4(cb + ((((uint32_t)qtr) ^ x7) << 4), pre[8].x, pre[8].y, pre[8].z, pre[8].w);
+                        st_shared_v4(cb + ((((uint32_t)qtr + 4u) ^ x7) << 4), pre[9].x, pre[9].y, pre[9].z,
+                                     pre[9].w);
+                    }
+                    if (c % 3 == 2) {
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(bar_grp + 8 * (c / 3));
+                    }
                 }
             }
-            fence_async_smem();
-            named_bar(3, kThreads);   // K tile of block b complete
+            // ---- next block's entries into registers; cache slots of block b + 2 (stored below)
             if (b + 1 < nblocks)
                 issue_loads(b + 1);
-            if (warp < 4 && b + 2 < nblocks) {
-                for (int k = tid - 32; k < kBK; k += 96)
-                    slots[((b + 2) % 3) * kBK + k] = slot_of(p, t, row, row_ok, kbeg, kend, b + 2, k);
+            int next_slot = -1;
+            if (wid < kBK && b + 2 < nblocks) {
+                const int i = kbeg + (b + 2) * kBK + wid;
+                if (i < kend)
+                    next_slot = slot_row[i];
             }
-            if (!is_soft)
-                continue;
-            // ---- softmax of block b (warps 4-11; this warp: lanes of its quadrant, heads 32hh..32hh+31)
+
+            // ---- softmax of block b: this warp's 32 keys (TMEM lanes) x 16 heads
             mbar_wait(bar_s, ph, flags, p.status);
             tc_after();
             const bool kv = (b * kBK + key < nkeys) && slots[(b % 3) * kBK + key] >= 0;
-            const uint32_t colS = kColS + 32 * hh;
-            {   // per-head maxima of this block over the 32 keys of the quadrant; lane j keeps head j
+            {   // per-head maxima over this warp's keys; lane j keeps head hs + j
+                uint32_t s[16];
+                tmem_ld16(lane_base + kColS + hs, s);
+                tmem_ld_wait();
                 float mine = -INFINITY;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t s[16];
-                    tmem_ld16(lane_base + colS + 16 * half, s);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float m = warp_max(kv ? __uint_as_float(s[j]) : -INFINITY);
-                        mine = lane == 16 * half + j ? m : mine;
-                    }
+                for (int j = 0; j < 16; ++j) {
+                    const float m = warp_max(kv ? __uint_as_float(s[j]) : -INFINITY);
+                    mine = lane == j ? m : mine;
                 }
-                red[quad * kNH + 32 * hh + lane] = mine;
+                if (lane < 16)
+                    red[quad * kNH + hs + lane] = mine;
             }
-            named_bar(1, kSoftThreads);
-            if (stid < kNH) {
-                const int h = stid;
+            named_bar(1, kWorkers);
+            if (wid < kNH) {
+                const int h = wid;
                 const float mb = fmaxf(fmaxf(red[h], red[kNH + h]), fmaxf(red[2 * kNH + h], red[3 * kNH + h]));
                 const float mo = mrun[h];
                 float mn = mo;
@@ -664,42 +827,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 mcs[h] = mn == -INFINITY ? 0.f : mn * c2;
                 alpha[h] = a;
             }
-            named_bar(1, kSoftThreads);
+            named_bar(1, kWorkers);
             if (flags[1] == b + 1) {   // some head's max grew past the threshold: rescale O^T and row sums
-                uint32_t x[16];
 #pragma unroll 1
-                for (int m = 0; m < 10; ++m) {   // four O^T tiles, then the row sums, 16 columns at a time
-                    const uint32_t col = ((m >> 1) < 4 ? kColO + 64 * (m >> 1) : kColL) + 32 * hh + 16 * (m & 1);
-                    tmem_ld16(lane_base + col, x);
+                for (int m = 0; m < 10; ++m) {   // four O^T tiles, then the row sums, 8 columns at a time
+                    const uint32_t col = ((m >> 1) < 4 ? kColO + 64 * (m >> 1) : kColL) + hs + 8 * (m & 1);
+                    uint32_t x[8];
+                    tmem_ld8(lane_base + col, x);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        x[j] = __float_as_uint(__uint_as_float(x[j]) * alpha[32 * hh + 16 * (m & 1) + j]);
-                    tmem_st16(lane_base + col, x);
+                    for (int j = 0; j < 8; ++j)
+                        x[j] = __float_as_uint(__uint_as_float(x[j]) * alpha[hs + 8 * (m & 1) + j]);
+                    tmem_st8(lane_base + col, x);
                 }
             }
             // P = 2^(s*c - m*c) -> BF16 P^T row `key`; row sums accumulate per lane in TMEM
-#pragma unroll 1
-            for (int hq = 0; hq < 2; ++hq) {   // 16 heads at a time
-                const int hb = 32 * hh + 16 * hq;
-                uint32_t sv[16], l[16];
-                tmem_ld16(lane_base + kColS + hb, sv);
-                if (b > 0)
-                    tmem_ld16(lane_base + kColL + hb, l);
-                tmem_ld_wait();
-                uint32_t pk[8];
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) {
+            for (int half = 0; half < 2; ++half) {
+                const int hb = hs + 8 * half;
+                uint32_t sv[8], l[8];
+                tmem_ld8(lane_base + kColS + hb, sv);
+                if (b > 0)
+                    tmem_ld8(lane_base + kColL + hb, l);
+                tmem_ld_wait();
+                uint32_t pk[4];
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
                     const float p0 = kv ? exp2f(fmaf(__uint_as_float(sv[j]), c2, -mcs[hb + j])) : 0.f;
                     const float p1 = kv ? exp2f(fmaf(__uint_as_float(sv[j + 1]), c2, -mcs[hb + j + 1])) : 0.f;
                     l[j] = __float_as_uint((b > 0 ? __uint_as_float(l[j]) : 0.f) + p0);
                     l[j + 1] = __float_as_uint((b > 0 ? __uint_as_float(l[j + 1]) : 0.f) + p1);
                     pk[j >> 1] = pack_bf16x2(p0, p1);
                 }
-                tmem_st16(lane_base + kColL + hb, l);
+                tmem_st8(lane_base + kColL + hb, l);
                 st_shared_v4(sP + sw128(key, hb >> 3), pk[0], pk[1], pk[2], pk[3]);
-                st_shared_v4(sP + sw128(key, (hb >> 3) + 1), pk[4], pk[5], pk[6], pk[7]);
             }
+            if (wid < kBK && b + 2 < nblocks)
+                slots[((b + 2) % 3) * kBK + wid] = next_slot;   // read after the next softmax barrier
             tmem_st_wait();
             fence_async_smem();
             tc_before();
@@ -707,36 +871,57 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             if (lane == 0)
                 mbar_arrive(bar_p);
         }
-    }
 
-    mbar_wait(bar_o, (uint32_t)((nblocks - 1) & 1), flags, p.status);
-    tc_after();
+        mbar_wait(bar_pv + 24, (uint32_t)((nblocks - 1) & 1), flags, p.status);
+        tc_after();
 
-    // ---- epilogue: row sums across lanes; normalised output, or the partial staged for the merge
-    float *lred = reinterpret_cast<float *>(gbase);   // Q region is free: [128 lanes][65]
-    if (is_soft) {
+        // ---- epilogue: row sums across the 128 lanes, then the normalised output or the staged partial
         {
-            uint32_t l[32];
-            tmem_ld32(lane_base + kColL + 32 * hh, l);
+            uint32_t lr[16];
+            tmem_ld16(lane_base + kColL + hs, lr);
             tmem_ld_wait();
+            float v[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                lred[key * 65 + 32 * hh + j] = __uint_as_float(l[j]);
-        }
-        named_bar(1, kSoftThreads);
-        if (stid < kNH) {
-            const int h = stid;
-            float acc[8];
+            for (int j = 0; j < 16; ++j)
+                v[j] = __uint_as_float(lr[j]);
+            // halving exchange: after the step with distance d the lane keeps half of its heads,
+            // summed with the partner's; at the end lane l holds head 8 b4 + 4 b3 + 2 b2 + b1
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
-                acc[a] = 0.f;
-#pragma unroll 2
-            for (int k = 0; k < kBK; k += 8) {
-#pragma unroll
-                for (int a = 0; a < 8; ++a)
-                    acc[a] += lred[(k + a) * 65 + h];
+            for (int k = 0; k < 8; ++k) {
+                const bool up = lane & 16;
+                const float give = up ? v[k] : v[k + 8];
+                const float keep = up ? v[k + 8] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
             }
-            const float lsum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const bool up = lane & 8;
+                const float give = up ? v[k] : v[k + 4];
+                const float keep = up ? v[k + 4] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const bool up = lane & 4;
+                const float give = up ? v[k] : v[k + 2];
+                const float keep = up ? v[k + 2] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+            }
+            {
+                const bool up = lane & 2;
+                const float give = up ? v[0] : v[1];
+                const float keep = up ? v[1] : v[0];
+                v[0] = keep + __shfl_xor_sync(0xffffffffu, give, 2);
+            }
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+            const int hsel = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+            if ((lane & 1) == 0)
+                red[quad * kNH + hs + hsel] = v[0];
+        }
+        named_bar(1, kWorkers);
+        if (wid < kNH) {
+            const int h = wid;
+            const float lsum = (red[h] + red[kNH + h]) + (red[2 * kNH + h] + red[3 * kNH + h]);
             const float m = mrun[h];
             const float ms = m == -INFINITY ? -INFINITY : m * p.scale;   // natural-log units
             if (p.splits == 1) {
@@ -755,23 +940,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 fin[h] = ms == -INFINITY ? 0.f : lsum;
             }
         }
-        named_bar(1, kSoftThreads);
-        uint32_t x[32];
+        named_bar(1, kWorkers);
+        {
+            uint32_t x[16];
 #pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-            const int dv = 128 * m + key;
-            tmem_ld32(lane_base + kColO + 64 * m + 32 * hh, x);
-            tmem_ld_wait();
-            if (p.splits == 1) {
+            for (int m = 0; m < 4; ++m) {
+                const int dv = 128 * m + key;
+                tmem_ld16(lane_base + kColO + 64 * m + hs, x);
+                tmem_ld_wait();
+                if (p.splits == 1) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int h = 32 * hh + j;
-                    p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] = bf16_bits(__uint_as_float(x[j]) * fin[h]);
+                    for (int j = 0; j < 16; ++j) {
+                        const int h = hs + j;
+                        p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] =
+                            bf16_bits(__uint_as_float(x[j]) * fin[h]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        o_stage[(hs + j) * kLatent + dv] = __uint_as_float(x[j]);
                 }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    o_stage[(32 * hh + j) * kLatent + dv] = __uint_as_float(x[j]);
             }
         }
     }
@@ -782,15 +970,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     if (p.splits > 1) {
         cluster_sync();   // every split has staged its partial
-        cluster_merge_pull(p, t, h0, split, smem_u32(alpha), smem_u32(fin), sK, wts);
+        cluster_merge_pull(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split, smem_u32(alpha), smem_u32(fin),
+                           sK, reinterpret_cast<float *>(gbase));
         cluster_sync();   // peers have finished reading this CTA's shared memory
     }
 }
 
 }  // namespace
 
-int decode_tc_chunk_keys() { return kBK; }
 int decode_tc_max_splits() { return kMaxSplits; }
+int decode_tc_block_keys() { return kBK; }
 
 // Concurrently resident CTAs of the decode kernel when launched in clusters of `splits`
 // (whole clusters must fit inside one GPC); cached per device.
@@ -835,7 +1024,8 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
 {
     if (p.num_tokens <= 0)
         return cudaSuccess;
-    if (p.heads_per_group != kNH || p.chunk % kBK != 0 || p.splits < 1 || p.splits > kMaxSplits)
+    if (p.heads_per_group != kNH || p.chunk <= 0 || p.splits < 1 || p.splits > kMaxSplits || p.topk_width < 0 ||
+        p.topk_width > kMaxTopkWidth || p.table_bits < 1 || (2 * sizeof(int) << p.table_bits) > (size_t)kKBytes)
         return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(decode_tc_kernel), kSmemBytes, kAttrTc);
     if (e != cudaSuccess)

@@ -51,7 +51,7 @@ struct DecodeParams {
     int32_t max_blocks;
     int32_t num_reqs;
     const int32_t *req_idx;
-    const int32_t *combined;   // [T, cw]
+    int32_t *combined;         // [T, cw]: combined lists (CUDA-core path) or cache slots (tensor-core path)
     int32_t cw;
     const int32_t *lens;       // [T]
     int32_t num_tokens;
@@ -67,6 +67,14 @@ struct DecodeParams {
     int32_t splits;
     int32_t chunk;
     unsigned *status;
+    // the combine's inputs, read by the tensor-core kernel, which combines in its prologue
+    const int32_t *topk;
+    int64_t topk_stride;
+    int32_t topk_width;
+    const int32_t *topk_lens;
+    const int32_t *seq_lens;
+    int32_t window;
+    int32_t table_bits;
 };
 
 // Raises a kernel's dynamic shared-memory limit to at least `bytes`, once per
@@ -91,7 +99,7 @@ cudaError_t launch_after_previous(const void *kernel, unsigned grid, unsigned bl
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
-int decode_tc_chunk_keys();
+int decode_tc_block_keys();
 int decode_tc_max_splits();
 int decode_tc_resident_ctas(int splits);
 int merge_max_splits();

@@ -4,9 +4,9 @@
 // captured or replayed pipeline whose memory was fixed up front, plug-ins whose host
 // framework owns every allocation, or environments where cudaMalloc is not allowed
 // between set-up and shutdown.  This entry point takes the decode's scratch (the
-// combined index lists, their lengths and, on the CUDA-core path, split partials) from
+// combined index lists or cache slots, their lengths and the split partials) from
 // one static device array compiled into the library instead of a workspace argument.
-// The array is kNoAllocScratchBytes (16 MiB) and exists on every GPU that loads the
+// The array is kNoAllocScratchBytes (32 MiB) and exists on every GPU that loads the
 // library until the process exits.
 #include <mutex>
 
@@ -16,7 +16,7 @@
 namespace dsv4 {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;
 
 // The scratch array.  In host code this name only stands for the symbol: its device
 // address comes from cudaGetSymbolAddress (once per device, below).
