@@ -20,22 +20,26 @@
 // chunks) is read by both: as K-major A for S^T and, without a copy, as MN-major A for O^T.
 // S^T, O^T (four 128-dv tiles) and per-lane partial row sums live in TMEM (512 columns).
 //
-// CTA = 16 warps, one (token, 64-head group, split).  Prologue: the CTA combines its
-// token's top-k row with the window (shared-memory hash set for first occurrences, block
-// scan for the output order), keeps the entries of its own split and resolves them through
-// the block table to cache slots: blocks 0 and 1 straight into shared memory, later blocks
-// into the workspace.  Per 128-key block:
-//   dequant   thread (row = tid / 4, quarter = tid % 4) holds its row's 16-byte pieces
-//             of the block in registers (loaded during the previous block) and writes the
-//             exact BF16 values chunk by chunk; chunk c of block b+1 is written as soon as
-//             the P.V product of block b has released it
-//   S^T       lane 0 of warp 0 issues the 4 MMAs of chunk c once every warp has written it,
-//             so the product trails the dequant by one chunk
+// CTA = 17 warps, one (token, 64-head group, split): warp 0 issues the MMAs, warps 1-16 do
+// everything else.  Prologue: the CTA combines its token's top-k row with the window
+// (shared-memory hash set for first occurrences, ballot scan for the output order), keeps the
+// entries of its own split and resolves them through the block-table row (cached in shared
+// memory) to cache slots: blocks 0 and 1 straight into shared memory, later blocks into the
+// workspace.  Per 128-key block:
+//   dequant   each worker thread owns a quarter of one row of the tile (the rows of a warp
+//             differ in row % 8 and spread over the tile), holds the row's 16-byte pieces
+//             in registers (loaded during the previous block) and writes the exact BF16
+//             values chunk by chunk; chunk c of block b+1 is written as soon as the P.V
+//             product of block b has released it; rows past the split's keys are zeros
+//   S^T       lane 0 of warp 0 issues the MMAs of each group of three column chunks once
+//             every worker warp has written it, so the product trails the dequant
 //   softmax   all 16 warps: warp w reads TMEM lanes 32 (w % 4).. (its keys) for heads
-//             16 (w / 4)..; per-head block maxima with redux.sync, lazy rescaling (only when
-//             a head's max grows by more than 2^8), P^T (BF16) into shared memory, row sums
-//             in TMEM
-//   O^T       32 MMAs, committed per 128-dv tile so the next block's dequant can start
+//             16 ((w - 1) / 4)..; per-head block maxima with redux.sync, one barrier to share
+//             them between the four warps of a head slice, which then each keep the running
+//             max in registers; lazy rescaling (only when a head's max grows by more than
+//             2^8), P^T (BF16) into shared memory, row sums in TMEM
+//   O^T       up to 32 MMAs (only the 16-key steps that hold keys), committed per 128-dv tile
+//             so the next block's dequant can start
 // When a token's keys are split over S CTAs (S <= 8), the S CTAs form a thread-block
 // cluster: each stages its partial in its own shared memory and, after a cluster
 // barrier, every CTA merges a slice of the heads by reading its peers' partials through
@@ -74,16 +78,17 @@ constexpr int kMaxSplits = 8;            // portable cluster size
 
 // small shared region (after Q and the K tile)
 constexpr int kOffSlots = 0;             // int [3][128]: cache slots of blocks b, b+1, b+2
-constexpr int kOffRed = 1536;            // float [4][64]
-constexpr int kOffMrun = 2560;           // float [64]
-constexpr int kOffMc = 2816;             // float [64]
-constexpr int kOffAlpha = 3072;          // float [64]
-constexpr int kOffFin = 3328;            // float [64]
-constexpr int kOffWsum = 3584;           // int [32]
-constexpr int kOffBars = 3712;           // u64: bar_s, bar_p, bar_pv[4], bar_grp[3]
-constexpr int kOffTmem = 3784;           // u32
-constexpr int kOffFlags = 3792;          // int [2]
-constexpr int kSmallBytes = 3840;
+constexpr int kOffRed = 1536;            // float [2][4][64]: per-quadrant head maxima, by block parity
+constexpr int kOffMrun = 3584;           // float [64]
+constexpr int kOffAlpha = 3840;          // float [64]
+constexpr int kOffFin = 4096;            // float [64]
+constexpr int kOffWsum = 4352;           // int [32]
+constexpr int kOffBars = 4480;           // u64: bar_s, bar_p, bar_pv[4], bar_grp[3]
+constexpr int kOffTmem = 4552;           // u32
+constexpr int kOffFlags = 4560;          // int [2]
+constexpr int kSmallBytes = 4608;
+constexpr int kBtOffset = 2 * 4 * 2 * kMaxTopkWidth;   // block-table cache in the K tile region, after the hash set
+constexpr int kBtCache = (kKBytes - kBtOffset) / 4;    // entries
 constexpr int kSmemBytes = kQBytes + kKBytes + kSmallBytes + 1024;   // + alignment slack
 constexpr int kQLoads = kNH * (kDim / 8) / kWorkers;                 // 9 16-byte Q pieces per worker
 constexpr int kGroups = 3;               // S^T is issued in 3 groups of 3 column chunks
@@ -282,8 +287,8 @@ __device__ __forceinline__ void dequant16_store(uint4 v, uint32_t se, uint32_t a
     }
     uint32_t bad = se > 134u ? 1u : 0u;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        bad |= ((t[i] & 0x7F007F00u) + 0x01000100u) & 0x80008000u;   // magnitude 0x7F present
+    for (int i = 0; i < 4; ++i)
+        bad |= ((w[i] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;   // a byte with magnitude 0x7F
     if (bad == 0u) {
         uint32_t f = (se + 120u) << 7;
         f |= f << 16;
@@ -443,12 +448,13 @@ __device__ __noinline__ void cluster_merge_pull(uint16_t *out, float *lse, const
 
 // Logical position -> cache slot (phys_block * page + offset) through the token's
 // block-table row; -1 (and the bad-index status bit) when the table has no valid block.
-__device__ __forceinline__ int slot_of_position(const DecodeParams &p, int row, int idx)
+__device__ __forceinline__ int slot_of_position(const DecodeParams &p, int row, int idx, const int *bt_s,
+                                                bool bt_cached)
 {
     const int blk = idx / p.page;
     int phys = -1;
     if (blk < p.max_blocks)
-        phys = p.block_table[(int64_t)row * p.bt_stride + blk];
+        phys = bt_cached ? bt_s[blk] : p.block_table[(int64_t)row * p.bt_stride + blk];
     if (phys < 0 || phys >= p.num_blocks) {
         atomicOr(p.status, kStatusBadIndex);
         return -1;
@@ -488,7 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     int *slots = reinterpret_cast<int *>(small + kOffSlots);
     float *red = reinterpret_cast<float *>(small + kOffRed);
     float *mrun = reinterpret_cast<float *>(small + kOffMrun);
-    float *mcs = reinterpret_cast<float *>(small + kOffMc);
     float *alpha = reinterpret_cast<float *>(small + kOffAlpha);   // at the end: this split's max per head
     float *fin = reinterpret_cast<float *>(small + kOffFin);       // at the end: this split's row sum per head
     int *wsum = reinterpret_cast<int *>(small + kOffWsum);
@@ -511,6 +516,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     }
     const int row = p.req_idx ? p.req_idx[t] : t;
     const bool row_ok = row >= 0 && row < p.num_reqs;
+    // the token's block-table row -> shared memory, read alongside the top-k row
+    int *bt_s = reinterpret_cast<int *>(gbase + kQBytes + kBtOffset);
+    const bool bt_cached = p.max_blocks <= kBtCache;
+    if (row_ok && bt_cached) {
+        const int32_t *bt_row = p.block_table + (int64_t)row * p.bt_stride;
+        for (int i = tid; i < p.max_blocks; i += kThreads)
+            bt_s[i] = __ldg(bt_row + i);
+    }
     const int32_t *trow = p.topk + (int64_t)t * p.topk_stride;
     const int npass = (n + kThreads - 1) / kThreads;   // the combine visits entry pass * kThreads + tid
     int tv[kPassLoads];
@@ -596,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             total += wsum[w];
         }
         if (keep && row_ok && rank >= kbeg && rank < klim) {
-            const int sl = slot_of_position(p, row, v);
+            const int sl = slot_of_position(p, row, v, bt_s, bt_cached);
             if (rank - kbeg < kHeadSlots)
                 slots[rank - kbeg] = sl;
             else
@@ -613,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         atomicOr(p.status, kStatusBadIndex);
     if (row_ok) {   // the window part of this split
         for (int i = max(kbeg, total) + tid; i < kend; i += kThreads) {
-            const int sl = slot_of_position(p, row, win_lo + (i - total));
+            const int sl = slot_of_position(p, row, win_lo + (i - total), bt_s, bt_cached);
             if (i - kbeg < kHeadSlots)
                 slots[i - kbeg] = sl;
             else
@@ -665,8 +678,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         flags[0] = 0;
         flags[1] = 0;
     }
-    if (tid < kNH)
-        mrun[tid] = -INFINITY;
     if (is_mma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(kTmemCols)
@@ -723,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         if (kk < ksteps)
                             umma(tmem + kColO + 64 * m, a + (uint64_t)(kk * 128), pv_b + (uint64_t)(kk * 128), kIdescPV,
-                             (b > 0 || kk > 0) ? 1u : 0u);
+                                 (b > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(bar_pv + 8 * m);   // releases K chunks 2m, 2m+1 (tile 3: also P^T)
                 }
             }
@@ -748,6 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             }
         };
         issue_loads(0);
+        float m_run = -INFINITY;   // running max (logit units) of head hs + lane % 16
 
         for (int b = 0; b < nblocks; ++b) {
             const uint32_t ph = (uint32_t)(b & 1);
@@ -796,39 +808,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             mbar_wait(bar_s, ph, flags, p.status);
             tc_after();
             const bool kv = (b * kBK + key < nkeys) && slots[(b % 3) * kBK + key] >= 0;
+            float *redb = red + (b & 1) * 4 * kNH;
             {   // per-head maxima over this warp's keys; lane j keeps head hs + j
-                uint32_t s[16];
-                tmem_ld16(lane_base + kColS + hs, s);
-                tmem_ld_wait();
                 float mine = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float m = warp_max(kv ? __uint_as_float(s[j]) : -INFINITY);
-                    mine = lane == j ? m : mine;
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sa[8];
+                    tmem_ld8(lane_base + kColS + hs + 8 * half, sa);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float m = warp_max(kv ? __uint_as_float(sa[j]) : -INFINITY);
+                        mine = lane == 8 * half + j ? m : mine;
+                    }
                 }
                 if (lane < 16)
-                    red[quad * kNH + hs + lane] = mine;
+                    redb[quad * kNH + hs + lane] = mine;
             }
             named_bar(1, kWorkers);
-            if (wid < kNH) {
-                const int h = wid;
-                const float mb = fmaxf(fmaxf(red[h], red[kNH + h]), fmaxf(red[2 * kNH + h], red[3 * kNH + h]));
-                const float mo = mrun[h];
-                float mn = mo;
+            // every warp forms the block maxima of its own 16 heads (lane j and j + 16: head hs + j);
+            // the four warps sharing the heads compute the same values, so the running max stays in
+            // registers and the rescale decision is per warp
+            float mcs_l, alpha_l;
+            {
+                const int hj = hs + (lane & 15);
+                const float mb = fmaxf(fmaxf(redb[hj], redb[kNH + hj]), fmaxf(redb[2 * kNH + hj], redb[3 * kNH + hj]));
                 float a = 1.f;
-                if (mo == -INFINITY) {
-                    mn = mb;
-                } else if (mb > mo && (mb - mo) * c2 > kRescaleLog2) {
-                    mn = mb;
-                    a = exp2f((mo - mb) * c2);
-                    flags[1] = b + 1;
+                if (m_run == -INFINITY) {
+                    m_run = mb;
+                } else if (mb > m_run && (mb - m_run) * c2 > kRescaleLog2) {
+                    a = exp2f((m_run - mb) * c2);
+                    m_run = mb;
                 }
-                mrun[h] = mn;
-                mcs[h] = mn == -INFINITY ? 0.f : mn * c2;
-                alpha[h] = a;
+                mcs_l = m_run == -INFINITY ? 0.f : m_run * c2;
+                alpha_l = a;
             }
-            named_bar(1, kWorkers);
-            if (flags[1] == b + 1) {   // some head's max grew past the threshold: rescale O^T and row sums
+            if (__any_sync(0xffffffffu, alpha_l != 1.f)) {   // a max grew past the threshold: rescale O^T, row sums
 #pragma unroll 1
                 for (int m = 0; m < 10; ++m) {   // four O^T tiles, then the row sums, 8 columns at a time
                     const uint32_t col = ((m >> 1) < 4 ? kColO + 64 * (m >> 1) : kColL) + hs + 8 * (m & 1);
@@ -837,7 +852,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        x[j] = __float_as_uint(__uint_as_float(x[j]) * alpha[hs + 8 * (m & 1) + j]);
+                        x[j] = __float_as_uint(__uint_as_float(x[j]) *
+                                               __shfl_sync(0xffffffffu, alpha_l, 8 * (m & 1) + j));
                     tmem_st8(lane_base + col, x);
                 }
             }
@@ -853,8 +869,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 uint32_t pk[4];
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
-                    const float p0 = kv ? exp2f(fmaf(__uint_as_float(sv[j]), c2, -mcs[hb + j])) : 0.f;
-                    const float p1 = kv ? exp2f(fmaf(__uint_as_float(sv[j + 1]), c2, -mcs[hb + j + 1])) : 0.f;
+                    const float m0 = __shfl_sync(0xffffffffu, mcs_l, 8 * half + j);
+                    const float m1 = __shfl_sync(0xffffffffu, mcs_l, 8 * half + j + 1);
+                    const float s0 = __uint_as_float(sv[j]);
+                    const float s1 = __uint_as_float(sv[j + 1]);
+                    const float p0 = kv ? exp2f(fmaf(s0, c2, -m0)) : 0.f;
+                    const float p1 = kv ? exp2f(fmaf(s1, c2, -m1)) : 0.f;
                     l[j] = __float_as_uint((b > 0 ? __uint_as_float(l[j]) : 0.f) + p0);
                     l[j + 1] = __float_as_uint((b > 0 ? __uint_as_float(l[j + 1]) : 0.f) + p1);
                     pk[j >> 1] = pack_bf16x2(p0, p1);
@@ -872,8 +892,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 mbar_arrive(bar_p);
         }
 
+        if (quad == 0 && lane < 16)
+            mrun[hs + lane] = m_run;
         mbar_wait(bar_pv + 24, (uint32_t)((nblocks - 1) & 1), flags, p.status);
         tc_after();
+        float *rede = red + (nblocks & 1) * 4 * kNH;   // the buffer the last block did not use
 
         // ---- epilogue: row sums across the 128 lanes, then the normalised output or the staged partial
         {
@@ -916,12 +939,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
             const int hsel = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
             if ((lane & 1) == 0)
-                red[quad * kNH + hs + hsel] = v[0];
+                rede[quad * kNH + hs + hsel] = v[0];
         }
         named_bar(1, kWorkers);
         if (wid < kNH) {
             const int h = wid;
-            const float lsum = (red[h] + red[kNH + h]) + (red[2 * kNH + h] + red[3 * kNH + h]);
+            const float lsum = (rede[h] + rede[kNH + h]) + (rede[2 * kNH + h] + rede[3 * kNH + h]);
             const float m = mrun[h];
             const float ms = m == -INFINITY ? -INFINITY : m * p.scale;   // natural-log units
             if (p.splits == 1) {
