@@ -41,9 +41,9 @@
 //   O^T       up to 32 MMAs (only the 16-key steps that hold keys), committed per 128-dv tile
 //             so the next block's dequant can start
 // When a token's keys are split over S CTAs (S <= 8), the S CTAs form a thread-block
-// cluster: each stages its partial in its own shared memory and, after a cluster
-// barrier, every CTA merges a slice of the heads by reading its peers' partials through
-// distributed shared memory.
+// cluster: after a cluster barrier each pushes its fp32 partial straight from TMEM into the
+// shared memory of the CTA that owns each head slice (distributed shared memory), and after
+// a second barrier every CTA merges its slice locally.
 // Every mbarrier wait is bounded; a wait that runs out records DSV4_ERR_TIMEOUT in the
 // status word and the CTA finishes without waiting again.
 #include <climits>
@@ -331,55 +331,37 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr)
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b)
 {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
 // Split-KV merge inside a cluster of S = splits CTAs (one per split of a token's keys).
-// Every CTA has staged, in its own shared memory, its running max m_s (natural-log
-// units, s_m[h]) and row sum l_s (s_l[h]) per head and its unnormalised O_s as fp32
-// [64 heads][512] (s_o).  After a cluster barrier the CTA of rank r merges heads
-// [r*hp, (r+1)*hp) (hp = ceil(64 / S)):
+// The CTA of rank r owns heads [r*hp, (r+1)*hp) (hp = ceil(64 / S)).  Every split s has
+// pushed, into each owner's shared memory, its running max m_s (natural-log units) and row
+// sum l_s for the owner's heads (stat[s][hl] = (m_s, l_s)) and its unnormalised fp32 O_s for
+// them (recv[s][hl][512]).  After the cluster barrier the owner forms
 //   m = max(max_s m_s, sink), Z = sum_s l_s e^{m_s - m} + e^{sink - m},
-//   out = sum_s e^{m_s - m} O_s / Z  (BF16),  lse = m + ln Z.
-// The statistics of all (head, split) pairs are pulled at once, one per thread; the O rows
-// are pulled two 16-byte pieces per thread at a time with the loads of all splits in flight.
-__device__ __noinline__ void cluster_merge_pull(uint16_t *out, float *lse, const float *sink, int num_heads, int S,
-                                                int t, int h0, int rank, uint32_t s_m, uint32_t s_l, uint32_t s_o,
-                                                float *scratch)
+//   out = sum_s e^{m_s - m} O_s / Z  (BF16),  lse = m + ln Z,
+// skipping splits without keys (weight 0, whatever their slots hold).
+__device__ __noinline__ void cluster_merge_local(uint16_t *out, float *lse, const float *sink, int num_heads, int S,
+                                                 int t, int h0, int rank, const float *recv, const float *stat,
+                                                 float *wts)
 {
     const int hp = (kNH + S - 1) / S;
     const int hb = rank * hp;
     const int nh = max(0, min(kNH, hb + hp) - hb);
     const int tid = threadIdx.x;
-    float *pm = scratch;            // [64][8] pulled maxima
-    float *pl = scratch + 512;      // [64][8] pulled row sums
-    float *wts = scratch + 1024;    // [64][10]: weight per split (divided by Z), then the lse
-    if (tid < nh * S) {
-        const int hl = tid / S;
-        const int s = tid % S;
-        pm[hl * 8 + s] = ld_cluster_f32(map_to_rank(s_m + 4u * (hb + hl), s));
-        pl[hl * 8 + s] = ld_cluster_f32(map_to_rank(s_l + 4u * (hb + hl), s));
-    }
-    __syncthreads();
     if (tid < nh) {
         const int h = hb + tid;
         float m = -INFINITY;
         for (int s = 0; s < S; ++s)
-            m = fmaxf(m, pm[tid * 8 + s]);
+            m = fmaxf(m, stat[2 * (s * hp + tid)]);
         const float mk = m;
         float sk = 0.f;
         if (sink != nullptr) {
@@ -388,10 +370,10 @@ __device__ __noinline__ void cluster_merge_pull(uint16_t *out, float *lse, const
         }
         float z = 0.f;
         for (int s = 0; s < S; ++s) {
-            const float ms = pm[tid * 8 + s];
+            const float ms = stat[2 * (s * hp + tid)];
             const float w = ms == -INFINITY ? 0.f : expf(ms - m);
             wts[tid * 10 + s] = w;
-            z += pl[tid * 8 + s] * w;
+            z += stat[2 * (s * hp + tid) + 1] * w;
         }
         if (sink != nullptr)
             z += expf(sk - m);
@@ -401,49 +383,38 @@ __device__ __noinline__ void cluster_merge_pull(uint16_t *out, float *lse, const
         wts[tid * 10 + 8] = z > 0.f ? m + logf(z) : -INFINITY;
     }
     __syncthreads();
-    uint32_t peer[kMaxSplits];
-#pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s)
-        peer[s] = s < S ? map_to_rank(s_o, s) : 0u;
     const int items = nh * (kLatent / 4);   // 16-byte pieces of the slice
-    for (int i = tid; i < items; i += 2 * kThreads) {
-        float4 v[2][kMaxSplits];
-        int hl[2], c[2];
-        bool ok[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int iu = i + u * kThreads;
-            ok[u] = iu < items;
-            hl[u] = ok[u] ? iu / (kLatent / 4) : 0;
-            c[u] = iu % (kLatent / 4);
-            const uint32_t off = (uint32_t)((hb + hl[u]) * kLatent + 4 * c[u]) * 4u;
-#pragma unroll
-            for (int s = 0; s < kMaxSplits; ++s)
-                v[u][s] = (ok[u] && s < S && wts[hl[u] * 10 + s] != 0.f) ? ld_cluster_v4(peer[s] + off)
-                                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            if (!ok[u])
-                continue;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int s = 0; s < kMaxSplits; ++s) {
-                const float ws = s < S ? wts[hl[u] * 10 + s] : 0.f;
-                acc.x = fmaf(ws, v[u][s].x, acc.x);
-                acc.y = fmaf(ws, v[u][s].y, acc.y);
-                acc.z = fmaf(ws, v[u][s].z, acc.z);
-                acc.w = fmaf(ws, v[u][s].w, acc.w);
+    for (int i = tid; i < items; i += kThreads) {
+        const int hl = i / (kLatent / 4);
+        const int c = i % (kLatent / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < S; ++s) {
+            const float ws = wts[hl * 10 + s];
+            if (ws != 0.f) {
+                const float4 v = *reinterpret_cast<const float4 *>(recv + ((size_t)(s * hp + hl)) * kLatent + 4 * c);
+                acc.x = fmaf(ws, v.x, acc.x);
+                acc.y = fmaf(ws, v.y, acc.y);
+                acc.z = fmaf(ws, v.z, acc.z);
+                acc.w = fmaf(ws, v.w, acc.w);
             }
-            uint2 o;
-            o.x = pack_bf16x2(acc.x, acc.y);
-            o.y = pack_bf16x2(acc.z, acc.w);
-            const int h = h0 + hb + hl[u];
-            *reinterpret_cast<uint2 *>(out + ((int64_t)t * num_heads + h) * kLatent + 4 * c[u]) = o;
-            if (c[u] == 0 && lse != nullptr)
-                lse[(int64_t)t * num_heads + h] = wts[hl[u] * 10 + 8];
         }
+        uint2 o;
+        o.x = pack_bf16x2(acc.x, acc.y);
+        o.y = pack_bf16x2(acc.z, acc.w);
+        const int h = h0 + hb + hl;
+        *reinterpret_cast<uint2 *>(out + ((int64_t)t * num_heads + h) * kLatent + 4 * c) = o;
+        if (c == 0 && lse != nullptr)
+            lse[(int64_t)t * num_heads + h] = wts[hl * 10 + 8];
     }
+}
+
+// Pushes the (m, l) pair of head h (0..63) of split `split` to the head's owner in the cluster.
+__device__ __forceinline__ void push_stat(uint32_t stat_s, int S, int split, int h, float m, float l)
+{
+    const int hp = (kNH + S - 1) / S;
+    const int r = h / hp;
+    const uint32_t off = (uint32_t)(2 * (split * hp + (h - r * hp))) * 4u;
+    st_cluster_v2(map_to_rank(stat_s + off, (uint32_t)r), m, l);
 }
 
 // Logical position -> cache slot (phys_block * page + offset) through the token's
@@ -503,7 +474,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const uint32_t bar_grp = bar_s + 48;                 // [3] column chunks 3g..3g+2 of the K tile written
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small + kOffTmem);
     volatile int *flags = reinterpret_cast<volatile int *>(small + kOffFlags);   // [0] abort, [1] rescale block tag
-    float *o_stage = reinterpret_cast<float *>(gbase + kQBytes);   // partial O [64][512] fp32 (K tile region)
     int *hkey = reinterpret_cast<int *>(gbase + kQBytes);          // combine hash set (K tile region)
 
     // ---- early loads: the token's sizes and top-k run first (the combine waits on them), then Q
@@ -646,14 +616,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             }
             return;
         }
-        if (tid < kNH) {   // an empty partial: weight 0 in the merge, its O is never read
-            alpha[tid] = -INFINITY;
-            fin[tid] = 0.f;
-        }
-        cluster_sync();   // every split has staged its partial
-        cluster_merge_pull(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split, smem_u32(alpha), smem_u32(fin),
-                           sK, reinterpret_cast<float *>(gbase));
-        cluster_sync();   // peers have finished reading this CTA's shared memory
+        cluster_sync();   // every split is past its matrix products: partials may land
+        if (tid < kNH)    // an empty partial: weight 0 in the merge, its O is never read
+            push_stat(smem_u32(gbase), p.splits, split, tid, -INFINITY, 0.f);
+        cluster_sync();   // every partial has landed
+        cluster_merge_local(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split,
+                            reinterpret_cast<const float *>(gbase + kQBytes), reinterpret_cast<const float *>(gbase),
+                            reinterpret_cast<float *>(gbase + 1024));
         return;
     }
 
@@ -964,24 +933,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             }
         }
         named_bar(1, kWorkers);
-        {
+        if (p.splits == 1) {
             uint32_t x[16];
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
                 const int dv = 128 * m + key;
                 tmem_ld16(lane_base + kColO + 64 * m + hs, x);
                 tmem_ld_wait();
-                if (p.splits == 1) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int h = hs + j;
-                        p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] =
-                            bf16_bits(__uint_as_float(x[j]) * fin[h]);
-                    }
-                } else {
+                for (int j = 0; j < 16; ++j) {
+                    const int h = hs + j;
+                    p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] = bf16_bits(__uint_as_float(x[j]) * fin[h]);
+                }
+            }
+        }
+    }
+    if (p.splits > 1) {
+        // the split's partial goes straight from TMEM into the shared memory of each head's owner:
+        // recv[split][head - owner's first head][512] in the owner's K tile region
+        cluster_sync();   // every split is past its matrix products: partials may land
+        if (!is_mma) {
+            const int S = p.splits;
+            const int hp = (kNH + S - 1) / S;
+            if (wid < kNH)
+                push_stat(smem_u32(gbase), S, split, wid, alpha[wid], fin[wid]);
+            const uint32_t recv_s = sK;
+            const int r0 = hs / hp;   // this warp's 16 heads belong to owners r0, r0 + 1, r0 + 2 at most
+            uint32_t x[16];
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
+                const int dv = 128 * m + key;
+                tmem_ld16(lane_base + kColO + 64 * m + hs, x);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        o_stage[(hs + j) * kLatent + dv] = __uint_as_float(x[j]);
+                for (int j = 0; j < 16; ++j) {
+                    const int h = hs + j;
+                    const int r = r0 + (h >= (r0 + 1) * hp) + (h >= (r0 + 2) * hp);
+                    const uint32_t off = (uint32_t)(((split * hp + h - r * hp) * kLatent + dv) * 4);
+                    if (r == split)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(recv_s + off), "f"(__uint_as_float(x[j])) : "memory");
+                    else
+                        st_cluster_f32(map_to_rank(recv_s + off, (uint32_t)r), __uint_as_float(x[j]));
                 }
             }
         }
@@ -992,10 +984,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     if (is_mma)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     if (p.splits > 1) {
-        cluster_sync();   // every split has staged its partial
-        cluster_merge_pull(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split, smem_u32(alpha), smem_u32(fin),
-                           sK, reinterpret_cast<float *>(gbase));
-        cluster_sync();   // peers have finished reading this CTA's shared memory
+        cluster_sync();   // every partial has landed
+        cluster_merge_local(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split,
+                            reinterpret_cast<const float *>(gbase + kQBytes), reinterpret_cast<const float *>(gbase),
+                            reinterpret_cast<float *>(gbase + 1024));
     }
 }
 
