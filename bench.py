@@ -404,9 +404,10 @@ def run_ours(args):
         "traffic": traffic_record(decode_kernel, w.name),
         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
         "kernel": decode_kernel,
-        "timed": "whole decode call per step (combine kernel + decode kernel with its split merge), CUDA "
-                 "events on the launching stream over the timed region; the decode kernel's own share of the "
-                 "step is in ncu_shares (committed ncu launch list)",
+        "timed": ("whole decode call per step (64/128 heads: the one kernel that combines, decodes and merges "
+                  "its splits; 16/32 heads: combine, decode and merge kernels), CUDA events on the launching "
+                  "stream over the timed region; per-kernel shares of the step are in ncu_shares (committed ncu "
+                  "launch list)"),
         "call_us": call_s * 1e6,
         "algorithmic_bytes_per_launch": bytes_per_step, "flops_per_launch": flops_per_step,
         "kv_gbs": bytes_per_step / call_s / 1e9, "tflops": flops_per_step / call_s / 1e12,
