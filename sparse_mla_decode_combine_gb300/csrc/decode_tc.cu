@@ -82,11 +82,11 @@ constexpr int kOffRed = 1536;            // float [2][4][64]: per-quadrant head 
 constexpr int kOffMrun = 3584;           // float [64]
 constexpr int kOffAlpha = 3840;          // float [64]
 constexpr int kOffFin = 4096;            // float [64]
-constexpr int kOffWsum = 4352;           // int [32]
-constexpr int kOffBars = 4480;           // u64: bar_s, bar_p, bar_pv[4], bar_grp[3]
-constexpr int kOffTmem = 4552;           // u32
-constexpr int kOffFlags = 4560;          // int [2]
-constexpr int kSmallBytes = 4608;
+constexpr int kOffWsum = 4352;           // int [4][32]
+constexpr int kOffBars = 4864;           // u64: bar_s, bar_p, bar_pv[4], bar_grp[3]
+constexpr int kOffTmem = 4936;           // u32
+constexpr int kOffFlags = 4944;          // int [2]
+constexpr int kSmallBytes = 4992;
 constexpr int kBtOffset = 2 * 4 * 2 * kMaxTopkWidth;   // block-table cache in the K tile region, after the hash set
 constexpr int kBtCache = (kKBytes - kBtOffset) / 4;    // entries
 constexpr int kSmemBytes = kQBytes + kKBytes + kSmallBytes + 1024;   // + alignment slack
@@ -507,8 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             const int i = wid + kWorkers * j;
             const int h = i / (kDim / 8);
             const int c = i % (kDim / 8);
-            qv[j] = __ldg(reinterpret_cast<const uint4 *>(p.q + (int64_t)t * p.q_token_stride +
-                                                           (int64_t)(h0 + h) * kDim + 8 * c));
+            qv[j] = ld_stream(p.q + (int64_t)t * p.q_token_stride + (int64_t)(h0 + h) * kDim + 8 * c);
         }
     }
 
@@ -552,40 +551,56 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             insert(v, i);
     }
     __syncthreads();
-    // survivors in input order: a ballot scan per pass; the ones of this split resolve to cache slots
+    // survivors in input order: ballots of up to four passes, one barrier, then every thread
+    // ranks its entries; the ones of this split resolve to cache slots
     const int kbeg = split * p.chunk;
     const int klim = kbeg + p.chunk;
     int32_t *slot_row = p.combined + (int64_t)t * p.cw;   // cache slots of blocks >= 2 of this split
     int total = 0;
 #pragma unroll 1
-    for (int ps = 0; ps < npass; ++ps) {
-        const int i = ps * kThreads + tid;
-        const int v = i < n ? __ldg(trow + i) : -1;   // cached by the first pass
-        bool keep = false;
-        if (v >= 0 && v < win_lo) {
-            unsigned h = hash_pos(v, bits);
-            while (hkey[h] != v)
-                h = (h + 1u) & (unsigned)(table - 1);
-            keep = hmin[h] == i;
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, keep);
-        if (lane == 0)
-            wsum[warp] = __popc(bal);
-        __syncthreads();
-        int rank = total + __popc(bal & ((1u << lane) - 1u));
+    for (int pg = 0; pg < npass; pg += kPassLoads) {
+        unsigned bal[kPassLoads];
+        int vg[kPassLoads];
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) {
-            rank += w < warp ? wsum[w] : 0;
-            total += wsum[w];
+        for (int u = 0; u < kPassLoads; ++u) {
+            bal[u] = 0;
+            vg[u] = -1;
+            if (pg + u >= npass)
+                continue;
+            const int i = (pg + u) * kThreads + tid;
+            const int v = pg == 0 ? tv[u] : (i < n ? __ldg(trow + i) : -1);
+            vg[u] = v;
+            bool keep = false;
+            if (v >= 0 && v < win_lo) {
+                unsigned h = hash_pos(v, bits);
+                while (hkey[h] != v)
+                    h = (h + 1u) & (unsigned)(table - 1);
+                keep = hmin[h] == i;
+            }
+            bal[u] = __ballot_sync(0xffffffffu, keep);
+            if (lane == 0)
+                wsum[32 * u + warp] = __popc(bal[u]);
         }
-        if (keep && row_ok && rank >= kbeg && rank < klim) {
-            const int sl = slot_of_position(p, row, v, bt_s, bt_cached);
-            if (rank - kbeg < kHeadSlots)
-                slots[rank - kbeg] = sl;
-            else
-                slot_row[rank] = sl;
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kPassLoads; ++u) {
+            if (pg + u >= npass)
+                continue;
+            int rank = total + __popc(bal[u] & ((1u << lane) - 1u));
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                rank += w < warp ? wsum[32 * u + w] : 0;
+                total += wsum[32 * u + w];
+            }
+            if (((bal[u] >> lane) & 1u) && row_ok && rank >= kbeg && rank < klim) {
+                const int sl = slot_of_position(p, row, vg[u], bt_s, bt_cached);
+                if (rank - kbeg < kHeadSlots)
+                    slots[rank - kbeg] = sl;
+                else
+                    slot_row[rank] = sl;
+            }
         }
-        __syncthreads();   // wsum is rewritten by the next pass
+        __syncthreads();   // wsum is rewritten by the next group of passes
     }
 
     const int L = total + swa;

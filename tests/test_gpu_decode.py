@@ -91,6 +91,34 @@ def test_decode_edge_lengths(heads, sink):
     compare_decode(out, lse, ref_out, ref_lse, what=f"edge h={heads} sink={sink}")
 
 
+@pytest.mark.parametrize("heads", [64, 128])
+def test_decode_junk_topk_entries(heads):
+    """Repeats (also across the 2176-entry passes of the fused combine), -1 padding, positions
+    past the token, positions inside the window and a topk_lens cut, in 3000-wide top-k rows."""
+    need_gpu()
+    rng = np.random.default_rng(41)
+    w = synth.make_workload(name="junk", seed=43, heads=heads, req_seq_lens=[5000, 4200, 300, 129, 2600],
+                            topk_width=3000, window=64, sink=True)
+    topk = w.topk_idx.copy()
+    T, K = topk.shape
+    for t in range(T):
+        pos = int(w.seq_lens[t]) - 1
+        row = topk[t]
+        m = rng.random(K)
+        src = rng.integers(0, K, size=K)
+        row[m < 0.2] = row[src[m < 0.2]]                                          # repeats anywhere in the row
+        row[(m >= 0.2) & (m < 0.3)] = -1
+        row[(m >= 0.3) & (m < 0.35)] = pos + 1 + rng.integers(0, 100, size=int(((m >= 0.3) & (m < 0.35)).sum()))
+        row[(m >= 0.35) & (m < 0.4)] = np.maximum(0, pos - rng.integers(0, 64, size=int(((m >= 0.35) & (m < 0.4)).sum())))
+        row[2500:2600] = row[100:200]                                             # repeats across passes
+    lens = np.array([K, 2900, 1000, 0, 2300], dtype=np.int32)
+    w = synth.Workload(**{**w.__dict__, "topk_idx": topk, "topk_lens": lens})
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(w)
+    compare_decode(out, lse, ref_out, ref_lse, what=f"junk top-k h={heads}")
+
+
 def test_decode_window_only_and_topk_only():
     need_gpu()
     w = small(5)
