@@ -31,8 +31,8 @@
 //             in registers (loaded during the previous block) and writes the exact BF16
 //             values chunk by chunk; chunk c of block b+1 is written as soon as the P.V
 //             product of block b has released it; rows past the split's keys are zeros
-//   S^T       lane 0 of warp 0 issues the MMAs of each group of three column chunks once
-//             every worker warp has written it, so the product trails the dequant
+//   S^T       lane 0 of warp 0 issues the MMAs of column chunks 0-5 once every worker warp
+//             has written them, then those of chunks 6-8, so the product trails the dequant
 //   softmax   all 16 warps: warp w reads TMEM lanes 32 (w % 4).. (its keys) for heads
 //             16 ((w - 1) / 4)..; per-head block maxima with redux.sync, one barrier to share
 //             them between the four warps of a head slice, which then each keep the running
@@ -83,7 +83,7 @@ constexpr int kOffMrun = 3584;           // float [64]
 constexpr int kOffAlpha = 3840;          // float [64]
 constexpr int kOffFin = 4096;            // float [64]
 constexpr int kOffWsum = 4352;           // int [4][32]
-constexpr int kOffBars = 4864;           // u64: bar_s, bar_p, bar_pv[4], bar_grp[3]
+constexpr int kOffBars = 4864;           // u64: bar_s, bar_p, bar_pv[4], bar_grp[2]
 constexpr int kOffTmem = 4936;           // u32
 constexpr int kOffFlags = 4944;          // int [2]
 constexpr int kSmallBytes = 4992;
@@ -91,7 +91,7 @@ constexpr int kBtOffset = 2 * 4 * 2 * kMaxTopkWidth;   // block-table cache in t
 constexpr int kBtCache = (kKBytes - kBtOffset) / 4;    // entries
 constexpr int kSmemBytes = kQBytes + kKBytes + kSmallBytes + 1024;   // + alignment slack
 constexpr int kQLoads = kNH * (kDim / 8) / kWorkers;                 // 9 16-byte Q pieces per worker
-constexpr int kGroups = 3;               // S^T is issued in 3 groups of 3 column chunks
+constexpr int kGroups = 2;               // S^T is issued in 2 groups: column chunks 0-5, then 6-8
 static_assert(kNH * (kDim / 8) % kWorkers == 0, "Q pieces per worker");
 static_assert(kKBytes >= 2 * (int)sizeof(int) * 2 * kMaxTopkWidth, "combine hash table fits the K tile");
 static_assert(kKBytes >= kNH * kLatent * (int)sizeof(float), "partial O fits the K tile");
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const uint32_t bar_s = smem_u32(small + kOffBars);   // S^T of the block complete
     const uint32_t bar_p = bar_s + 8;                    // P^T and row sums of the block written (16 warps)
     const uint32_t bar_pv = bar_s + 16;                  // [4] O^T tiles 0..m of the block complete
-    const uint32_t bar_grp = bar_s + 48;                 // [3] column chunks 3g..3g+2 of the K tile written
+    const uint32_t bar_grp = bar_s + 48;                 // [2] column chunks 0-5, then 6-8 of the K tile written
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small + kOffTmem);
     volatile int *flags = reinterpret_cast<volatile int *>(small + kOffFlags);   // [0] abort, [1] rescale block tag
     int *hkey = reinterpret_cast<int *>(gbase + kQBytes);          // combine hash set (K tile region)
@@ -695,10 +695,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             if (lane == 0) {
 #pragma unroll
                 for (int g = 0; g < kGroups; ++g) {
-                    mbar_wait_one(bar_grp + 8 * g, ph, flags, p.status);   // chunks 3g..3g+2 written
+                    mbar_wait_one(bar_grp + 8 * g, ph, flags, p.status);   // chunks of group g written
                     tc_after();
 #pragma unroll
-                    for (int c = 3 * g; c < 3 * g + 3; ++c) {
+                    for (int c = 6 * g; c < (g == 0 ? 6 : kChunks); ++c) {
                         const uint64_t a = qk_a + (uint64_t)((c * kChunkBytes) >> 4);
                         const uint64_t bq = qk_b + (uint64_t)((c * kQChunkBytes) >> 4);
 #pragma unroll
@@ -770,20 +770,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                         st_shared_v4(cb + ((((uint32_t)qtr + 4u) ^ x7) << 4), pre[9].x, pre[9].y, pre[9].z,
                                      pre[9].w);
                     }
-                    if (c % 3 == 2) {
+                    if (c == 5 || c == kChunks - 1) {
                         fence_async_smem();
                         __syncwarp();
                         if (lane == 0)
-                            mbar_arrive(bar_grp + 8 * (c / 3));
+                            mbar_arrive(bar_grp + 8 * (c == 5 ? 0 : 1));
                     }
                 }
             }
             // ---- next block's entries into registers; cache slots of block b + 2 (stored below)
             if (b + 1 < nblocks)
                 issue_loads(b + 1);
+            // cache slots of block b + 2: eight per worker warp (lanes 0-7), spread over all warps
+            const int ns = 8 * (warp - 1) + lane;
             int next_slot = -1;
-            if (wid < kBK && b + 2 < nblocks) {
-                const int i = kbeg + (b + 2) * kBK + wid;
+            if (lane < 8 && b + 2 < nblocks) {
+                const int i = kbeg + (b + 2) * kBK + ns;
                 if (i < kend)
                     next_slot = slot_row[i];
             }
@@ -866,8 +868,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 tmem_st8(lane_base + kColL + hb, l);
                 st_shared_v4(sP + sw128(key, hb >> 3), pk[0], pk[1], pk[2], pk[3]);
             }
-            if (wid < kBK && b + 2 < nblocks)
-                slots[((b + 2) % 3) * kBK + wid] = next_slot;   // read after the next softmax barrier
+            if (lane < 8 && b + 2 < nblocks)
+                slots[((b + 2) % 3) * kBK + ns] = next_slot;   // read after the next softmax barrier
             tmem_st_wait();
             fence_async_smem();
             tc_before();
