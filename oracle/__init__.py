@@ -71,6 +71,8 @@ class Oracle:
         lib.oracle_dequant_entry.argtypes = [P, P]
         lib.oracle_combine.restype = ctypes.c_int
         lib.oracle_combine.argtypes = [P, i64, i32, P, P, i32, i32, P, i64, i32, P]
+        lib.oracle_combine_compressed.restype = ctypes.c_int
+        lib.oracle_combine_compressed.argtypes = [P, i64, i32, P, P, P, i32, i32, i32, i32, i32, i32, P, i64, i32, P]
         lib.oracle_attend.restype = None
         lib.oracle_attend.argtypes = [P, P, i32, f64, ctypes.c_int, f64, P, P]
         lib.oracle_merge.restype = None
@@ -107,6 +109,23 @@ class Oracle:
                                      int(window), _ptr(out), combined_width, combined_width, _ptr(lens))
         if rc != 0:
             raise ValueError("combined_width too small")
+        return out, lens
+
+    def combine_compressed(self, topk_idx, query_start_loc, seq_lens, gather_lens, region_stride: int,
+                           compressed_len: int, top_k: int, compress_ratio: int, window: int, combined_width: int):
+        """Compressed-region combine -> (combined int32 [T, width], combined_lens int32 [T])."""
+        tk = _c(topk_idx, np.int32)
+        T, K = tk.shape
+        qsl = _c(query_start_loc, np.int32)
+        R = qsl.size - 1
+        out = np.empty((T, combined_width), dtype=np.int32)
+        lens = np.empty(T, dtype=np.int32)
+        rc = self.lib.oracle_combine_compressed(_ptr(tk), K, K, _ptr(qsl), _ptr(_c(seq_lens, np.int32)),
+                                                _ptr(_c(gather_lens, np.int32)), R, int(region_stride),
+                                                int(compressed_len), int(top_k), int(compress_ratio), int(window),
+                                                _ptr(out), combined_width, combined_width, _ptr(lens))
+        if rc != 0:
+            raise ValueError("arguments outside the compressed combine's rules")
         return out, lens
 
     def attend(self, q, keys, softmax_scale: float, sink: Optional[float] = None):
@@ -186,6 +205,12 @@ def dequant_entry(entry):
 
 def combine(topk_idx, topk_lens, seq_lens, window, combined_width):
     return default().combine(topk_idx, topk_lens, seq_lens, window, combined_width)
+
+
+def combine_compressed(topk_idx, query_start_loc, seq_lens, gather_lens, region_stride, compressed_len, top_k,
+                       compress_ratio, window, combined_width):
+    return default().combine_compressed(topk_idx, query_start_loc, seq_lens, gather_lens, region_stride,
+                                        compressed_len, top_k, compress_ratio, window, combined_width)
 
 
 def attend(q, keys, softmax_scale, sink=None):

@@ -99,6 +99,61 @@ void oracle_dequant_entry(const uint8_t *entry, double *k)
     }
 }
 
+/* Compressed-region combine: the page's full variant of the combine ("[ROCm] [DSv4] [Perf]
+ * Support DeepSeek v4 MTP", vllm #43385, section 关键源码片段 / rocm.py,
+ * _combine_topk_swa_indices_kernel).  Each request b owns a gathered region of M entries:
+ * N compressed entries (what top-k indexes), then raw positions from
+ * gather_start = seq_len - gather_len on.  Its tokens are [query_start_loc[b], ...[b + 1])
+ * (relative to query_start_loc[0]); token i of a request of query_len tokens sits at
+ * pos = seq_len - query_len + i and gets
+ *   topk_len = min((pos + 1) / C, TOP_K) entries  M*b + v  for its top-k values v in [0, N)
+ *                                                 (-1 for any other value, kept in place),
+ *   swa_len  = min(pos + 1, W) window entries       M*b + N + (pos - swa_len + 1 - gather_start) + j,
+ * length topk_len + swa_len.  No dedup: the two parts index different regions.
+ * Readings: a token with pos + 1 <= 0 gets no entries (the page's integer arithmetic would give a
+ * negative length); entries past the length are -1 (the page leaves them unwritten); TOP_K must
+ * not exceed the top-k row width (so the page's fallback read of entry 0 for offsets past the
+ * row never happens).  Returns 0, or 1 for arguments outside those rules. */
+int oracle_combine_compressed(const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width,
+                              const int32_t *query_start_loc, const int32_t *seq_lens, const int32_t *gather_lens,
+                              int32_t num_reqs, int32_t region_stride, int32_t compressed_len, int32_t top_k,
+                              int32_t compress_ratio, int32_t window, int32_t *combined, int64_t combined_stride,
+                              int32_t combined_width, int32_t *combined_lens)
+{
+    if (top_k < 0 || top_k > topk_width || compress_ratio < 1 || window < 0 || combined_width < top_k + window)
+        return 1;
+    const int64_t base = query_start_loc[0];
+    for (int32_t b = 0; b < num_reqs; ++b) {
+        const int64_t qs = query_start_loc[b] - base;
+        const int64_t qe = query_start_loc[b + 1] - base;
+        const int64_t start_pos = (int64_t)seq_lens[b] - (qe - qs);
+        const int64_t gather_start = (int64_t)seq_lens[b] - gather_lens[b];
+        const int64_t region = (int64_t)region_stride * b;
+        for (int64_t t = qs; t < qe; ++t) {
+            const int64_t pos = start_pos + (t - qs);
+            int64_t tk = 0, sw = 0;
+            if (pos + 1 > 0) {
+                tk = (pos + 1) / compress_ratio;
+                if (tk > top_k)
+                    tk = top_k;
+                sw = pos + 1 < window ? pos + 1 : window;
+            }
+            int32_t *row = combined + t * combined_stride;
+            const int32_t *in = topk_idx + t * topk_stride;
+            for (int64_t k = 0; k < tk; ++k) {
+                const int32_t v = in[k];
+                row[k] = (v >= 0 && v < compressed_len) ? (int32_t)(region + v) : -1;
+            }
+            for (int64_t j = 0; j < sw; ++j)
+                row[tk + j] = (int32_t)(region + compressed_len + (pos - sw + 1 - gather_start) + j);
+            for (int64_t k = tk + sw; k < combined_width; ++k)
+                row[k] = -1;
+            combined_lens[t] = (int32_t)(tk + sw);
+        }
+    }
+    return 0;
+}
+
 /* Combined index list of one token.  Returns its length L; row[0..L) holds
  * the kept top-k entries then the window, row[L..width) is -1. */
 int oracle_combine_token(const int32_t *topk_row, int32_t n_topk, int32_t seq_len, int32_t window,

@@ -379,8 +379,85 @@ def check_topk_lens_truncation(orc):
     assert not np.array_equal(a[1], c[1])
 
 
+# ----------------------------------------------------------------------------
+# compressed-region combine
+# ----------------------------------------------------------------------------
+GOLDEN_COMPRESSED = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                                 "combine_compressed_worked_examples.txt")
+
+
+def load_golden_compressed():
+    examples, cur = [], None
+    with open(GOLDEN_COMPRESSED) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            if key == "example":
+                cur = dict(name=rest, requests=[], tokens=[])
+            elif key == "params":
+                cur["M"], cur["N"], cur["top_k"], cur["C"], cur["W"], cur["width"] = [int(v) for v in rest.split()]
+            elif key == "request":
+                cur["requests"].append([int(v) for v in rest.split()])
+            elif key == "token":
+                topk, row, ln = [p.strip() for p in rest.split("|")]
+                cur["tokens"].append(([int(v) for v in topk.split()], [int(v) for v in row.split()], int(ln)))
+            elif key == "end":
+                examples.append(cur)
+    return examples
+
+
+def check_combine_compressed_golden(orc):
+    for ex in load_golden_compressed():
+        qlens = [r[0] for r in ex["requests"]]
+        qsl = np.array([100] + list(100 + np.cumsum(qlens)), dtype=np.int32)
+        width = max(len(t[0]) for t in ex["tokens"])
+        topk = np.array([t[0] + [-1] * (width - len(t[0])) for t in ex["tokens"]], dtype=np.int32)
+        row, ln = orc.combine_compressed(topk, qsl, [r[1] for r in ex["requests"]], [r[2] for r in ex["requests"]],
+                                         ex["M"], ex["N"], ex["top_k"], ex["C"], ex["W"], ex["width"])
+        for i, (_, want, wl) in enumerate(ex["tokens"]):
+            assert row[i].tolist() == want, (ex["name"], i, row[i].tolist(), want)
+            assert int(ln[i]) == wl, (ex["name"], i)
+
+
+def check_combine_compressed_invariants(orc):
+    """Random batches: lengths follow min((pos+1)//C, TOP_K) + min(pos+1, W); the window part is a
+    run of consecutive entries ending at the token's own position in its request's region; top-k
+    entries keep their order and map into [M*b, M*b + N) or to -1; the rest is -1."""
+    rng = np.random.default_rng(31)
+    for _ in range(60):
+        R = int(rng.integers(1, 6))
+        qlens = rng.integers(0, 4, size=R)
+        seqs = rng.integers(0, 300, size=R)
+        gl = np.minimum(seqs, rng.integers(0, 300, size=R) + 20)
+        M, N, top_k, C, W = 1000, int(rng.integers(1, 200)), int(rng.integers(0, 40)), int(rng.integers(1, 9)), int(rng.integers(0, 30))
+        T = int(qlens.sum())
+        K = top_k + int(rng.integers(0, 5))
+        topk = rng.integers(-3, N + 3, size=(max(T, 1), K)).astype(np.int32)[:T]
+        qsl = np.concatenate([[7], 7 + np.cumsum(qlens)]).astype(np.int32)
+        width = top_k + W + int(rng.integers(0, 4))
+        row, ln = orc.combine_compressed(topk.reshape(T, K), qsl, seqs, gl, M, N, top_k, C, W, width)
+        t = 0
+        for b in range(R):
+            for i in range(int(qlens[b])):
+                pos = int(seqs[b]) - int(qlens[b]) + i
+                tk = min((pos + 1) // C, top_k) if pos + 1 > 0 else 0
+                sw = min(pos + 1, W) if pos + 1 > 0 else 0
+                assert int(ln[t]) == tk + sw
+                for k in range(tk):
+                    v = int(topk[t, k])
+                    assert row[t, k] == (M * b + v if 0 <= v < N else -1)
+                win = row[t, tk:tk + sw]
+                if sw:
+                    assert np.all(np.diff(win) == 1)
+                    assert int(win[-1]) == M * b + N + pos - (int(seqs[b]) - int(gl[b]))
+                assert np.all(row[t, tk + sw:] == -1)
+                t += 1
+
+
 ALL_CHECKS = [check_e4m3_codes, check_ue8m0, check_bf16, check_entry_layout, check_quantize_roundtrip,
               check_combine_golden, check_combine_bruteforce, check_combine_config1_lengths,
               check_dense_equivalence, check_order_padding_invariance, check_page_permutation, check_closed_forms,
               check_lse_identity_and_sink_limit, check_merge_partition, check_empty_and_bad_index,
-              check_topk_lens_truncation]
+              check_topk_lens_truncation, check_combine_compressed_golden, check_combine_compressed_invariants]

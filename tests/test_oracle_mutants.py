@@ -39,6 +39,15 @@ MUTANTS = [
     ("merge weights against the max", "double w = exp(lse_parts[c] - l);", "double w = exp(lse_parts[c] - m);"),
     ("lse without the log", "double l = m + log(z);\n    for (int32_t j", "double l = m + z;\n    for (int32_t j"),
     ("softmax scale dropped", "s[j] = softmax_scale * acc;", "s[j] = acc;"),
+    ("compressed: position off by one", "const int64_t pos = start_pos + (t - qs);", "const int64_t pos = start_pos + (t - qs) + 1;"),
+    ("compressed: ratio applied to pos", "tk = (pos + 1) / compress_ratio;", "tk = pos / compress_ratio;"),
+    ("compressed: region offset dropped", "row[k] = (v >= 0 && v < compressed_len) ? (int32_t)(region + v) : -1;",
+     "row[k] = (v >= 0 && v < compressed_len) ? (int32_t)v : -1;"),
+    ("compressed: gather start ignored", "(pos - sw + 1 - gather_start) + j);", "(pos - sw + 1) + j);"),
+    ("compressed: window before the compressed part", "(int32_t)(region + compressed_len + (pos - sw + 1 - gather_start) + j)",
+     "(int32_t)(region + (pos - sw + 1 - gather_start) + j)"),
+    ("compressed: invalid top-k compacted", "row[k] = (v >= 0 && v < compressed_len) ? (int32_t)(region + v) : -1;",
+     "row[k] = (v >= 0 && v <= compressed_len) ? (int32_t)(region + v) : -1;"),
 ]
 
 
