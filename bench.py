@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["decode", "combine-compressed"], default="decode",
+                    help="decode (the headline) or the compressed-region combine on its own")
     ap.add_argument("--replicas", type=int, default=0,
                     help="workload replicas to rotate through (default: enough for 4x the L2)")
     return ap.parse_args()
@@ -490,8 +492,104 @@ def run_ours(args):
     return 0
 
 
+def run_combine_compressed(args):
+    """The compressed-region combine on its own: 64 requests x 4 tokens (speculative verify
+    shape), top-k 2048 of a 4x-compressed region, window 128, rows of 2304 entries. Bytes per
+    token: the top-k entries read (4 * topk_len) plus the row and length written (4 * width + 4)."""
+    import torch
+    import sparse_mla_decode_combine_gb300 as pkg
+    from sparse_mla_decode_combine_gb300 import build as pkg_build
+    pkg_build.build()
+    pkg.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rng = np.random.default_rng(1)
+    R, qlen, top_k, C, W, width = 64, 4, 2048, 4, 128, 2304
+    seqs = rng.integers(8192, 65536, size=R).astype(np.int32)
+    gls = np.full(R, W + qlen, dtype=np.int32)
+    N = 65536 // C
+    M = N + int(gls.max())
+    T = R * qlen
+    # replicas of the batch so that one rotation moves more than 4x the L2
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    pos = np.repeat(seqs, qlen) - qlen + np.tile(np.arange(qlen), R)
+    tk = np.minimum((pos + 1) // C, top_k)
+    sw = np.minimum(pos + 1, W)
+    bytes_per_step = int((4 * tk).sum() + T * (4 * width + 4))
+    reps = max(2, math.ceil(4 * l2 / bytes_per_step))
+    qsl = torch.from_numpy((np.arange(R + 1) * qlen).astype(np.int32)).to(dev)
+    s_d = torch.from_numpy(seqs).to(dev)
+    g_d = torch.from_numpy(gls).to(dev)
+    ins = [torch.from_numpy(rng.integers(-1, N, size=(T, top_k)).astype(np.int32)).to(dev) for _ in range(reps)]
+    outs = [torch.empty((T, width), dtype=torch.int32, device=dev) for _ in range(reps)]
+    lens = [torch.empty((T,), dtype=torch.int32, device=dev) for _ in range(reps)]
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        pkg.check(pkg.dsv4_combine_topk_swa_indices_compressed(ins[i % reps], qsl, s_d, g_d, M, N, top_k, C, W,
+                                                               outs[i % reps], lens[i % reps], stream=stream))
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            step(i)
+    torch.cuda.synchronize()
+    # one rotation over the replicas as a CUDA graph, replayed (the host does not pace the GPU),
+    # then a shorter graph for the last K mod replicas steps, so that exactly K steps are timed
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        return g
+    graph = capture(reps)
+    replays, rem = divmod(max(args.steps, 1), reps)
+    tail = capture(rem) if rem else None
+    torch.cuda.synchronize()
+    steps = replays * reps + rem
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    sampler.start()
+    time.sleep(0.2)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        if tail is not None:
+            tail.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    args.steps = steps
+    ms = ev0.elapsed_time(ev1)
+    step_s = ms / 1e3 / args.steps
+    hbm_peak, _, _, peak_src = peaks()
+    ach = bytes_per_step / step_s / 1e9
+    line = {"metric": "compressed-region combine query-tokens/s (bytes moved vs HBM roofline)",
+            "value": T / step_s, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int32", "data": "synthetic",
+            "config": {"workload": "compressed combine: 64 requests x 4 tokens, top-k 2048 of a 4x-compressed "
+                                   "region, window 128, rows of 2304", "tokens_per_step": T, "replicas": reps,
+                       "l2": f"inputs larger than L2: {reps} rotating replicas"},
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                         "traffic": None, "kernel": "combine_compressed_kernel",
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+                         "algorithmic_bytes_per_launch": bytes_per_step,
+                         "timed": "one call (one launch) per step, CUDA events on the launching stream"},
+            "gpu_launches": args.steps, "launches_per_step": 1, "clocks": sampler.summary(t0, t1)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.op == "combine-compressed":
+        if args.impl == "reference" or int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        return run_combine_compressed(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -112,6 +112,48 @@ DSV4_API dsv4_status dsv4_combine_topk_swa_indices(const int32_t *topk_idx, int6
                                           int32_t combined_width, int32_t *combined_lens, dsv4_stream_t stream);
 
 /*
+ * dsv4_combine_topk_swa_indices_compressed -- per-token index lists over a compressed region
+ * plus the raw window, for batches of multi-token requests (prefill chunks, speculative verify).
+ *
+ * Source: vllm #43385 "[ROCm] [DSv4] [Perf] Support DeepSeek v4 MTP", section
+ * "关键源码片段 / rocm.py", _combine_topk_swa_indices_kernel with COMPRESS_RATIO, gather_lens
+ * and query_start_loc.  Request b owns a gathered region of region_stride (M) entries:
+ * compressed_len (N) compressed entries, which top-k indexes, then the raw positions from
+ * gather_start = seq_lens[b] - gather_lens[b] on.  Its tokens are rows
+ * [query_start_loc[b] - query_start_loc[0], query_start_loc[b + 1] - query_start_loc[0]);
+ * token i of a request with query_len tokens sits at pos = seq_lens[b] - query_len + i and gets
+ *   topk_len = min((pos + 1) / compress_ratio, top_k)   (0 when pos + 1 <= 0)
+ *   swa_len  = min(pos + 1, window)                      (0 when pos + 1 <= 0)
+ *   combined[t][k]            = M*b + topk_idx[t][k] when 0 <= topk_idx[t][k] < N, else -1
+ *                               (k < topk_len; invalid entries stay in place, -1)
+ *   combined[t][topk_len + j] = M*b + N + (pos - swa_len + 1 - gather_start) + j   (j < swa_len)
+ *   combined[t][topk_len + swa_len .. combined_width) = -1
+ *   combined_lens[t]          = topk_len + swa_len
+ * The two parts index different regions, so nothing is deduplicated.  The arithmetic is 32-bit
+ * two's complement, as on the page.
+ *
+ * Arguments:
+ *   topk_idx         int32 [num_tokens, topk_width], row stride topk_stride (>= topk_width);
+ *                    may be NULL when top_k == 0.
+ *   query_start_loc  int32 [num_reqs + 1], non-decreasing, query_start_loc[num_reqs] -
+ *                    query_start_loc[0] == num_tokens (rows no request covers are set to -1
+ *                    with length 0 and flag DSV4_ERR_BAD_INDEX in the device status word).
+ *   seq_lens, gather_lens  int32 [num_reqs].
+ *   num_reqs         >= 0; num_tokens >= 0 (either 0 enqueues nothing).
+ *   region_stride, compressed_len  >= 0, region_stride * num_reqs < 2^31.
+ *   top_k            0 .. topk_width (<= 8192); compress_ratio >= 1; window >= 0.
+ *   combined         int32 [num_tokens, combined_width], row stride combined_stride
+ *                    (>= combined_width); combined_width >= top_k + window.
+ *   combined_lens    int32 [num_tokens].
+ * Returns DSV4_OK, DSV4_ERR_INVALID_ARG, DSV4_ERR_UNSUPPORTED (topk_width > 8192) or DSV4_ERR_CUDA.
+ */
+DSV4_API dsv4_status dsv4_combine_topk_swa_indices_compressed(
+    const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width, const int32_t *query_start_loc,
+    const int32_t *seq_lens, const int32_t *gather_lens, int32_t num_reqs, int32_t num_tokens, int32_t region_stride,
+    int32_t compressed_len, int32_t top_k, int32_t compress_ratio, int32_t window, int32_t *combined,
+    int64_t combined_stride, int32_t combined_width, int32_t *combined_lens, dsv4_stream_t stream);
+
+/*
  * dsv4_sparse_mla_decode_workspace_size -- bytes of device workspace dsv4_sparse_mla_decode needs.
  *
  * The size depends on the arguments and on the multiprocessor count of the current

@@ -29,8 +29,9 @@ DSV4_ERR_UNSUPPORTED = 5
 STATUS_NAMES = {0: "DSV4_OK", 1: "DSV4_ERR_INVALID_ARG", 2: "DSV4_ERR_BAD_INDEX", 3: "DSV4_ERR_TIMEOUT",
                 4: "DSV4_ERR_CUDA", 5: "DSV4_ERR_UNSUPPORTED"}
 
-EXPORTED = ("dsv4_combine_topk_swa_indices", "dsv4_sparse_mla_decode_workspace_size", "dsv4_sparse_mla_decode",
-            "dsv4_sparse_mla_decode_noalloc", "dsv4_get_device_status")
+EXPORTED = ("dsv4_combine_topk_swa_indices", "dsv4_combine_topk_swa_indices_compressed",
+            "dsv4_sparse_mla_decode_workspace_size", "dsv4_sparse_mla_decode", "dsv4_sparse_mla_decode_noalloc",
+            "dsv4_get_device_status")
 
 
 class Dsv4Error(RuntimeError):
@@ -63,6 +64,9 @@ def load_library():
     P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     lib.dsv4_combine_topk_swa_indices.restype = ctypes.c_int
     lib.dsv4_combine_topk_swa_indices.argtypes = [P, i64, i32, P, P, i32, i32, P, i64, i32, P, P]
+    lib.dsv4_combine_topk_swa_indices_compressed.restype = ctypes.c_int
+    lib.dsv4_combine_topk_swa_indices_compressed.argtypes = [P, i64, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                             P, i64, i32, P, P]
     lib.dsv4_sparse_mla_decode_workspace_size.restype = ctypes.c_size_t
     lib.dsv4_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.dsv4_sparse_mla_decode.restype = ctypes.c_int
@@ -115,6 +119,26 @@ def dsv4_combine_topk_swa_indices(topk_idx: torch.Tensor, topk_lens: Optional[to
         _ptr(topk_idx) if K > 0 else None, max(topk_idx.stride(0), K), K, _ptr(topk_lens), _ptr(seq_lens), T,
         int(window), _ptr(combined), max(combined.stride(0), combined.shape[1]), combined.shape[1],
         _ptr(combined_lens), _stream(stream))
+
+
+def dsv4_combine_topk_swa_indices_compressed(topk_idx: torch.Tensor, query_start_loc: torch.Tensor,
+                                             seq_lens: torch.Tensor, gather_lens: torch.Tensor, region_stride: int,
+                                             compressed_len: int, top_k: int, compress_ratio: int, window: int,
+                                             combined: torch.Tensor, combined_lens: torch.Tensor, stream=None) -> int:
+    """topk_idx int32 [T, K]; query_start_loc int32 [R + 1]; seq_lens, gather_lens int32 [R];
+    combined int32 [T, C] (C >= top_k + window); combined_lens int32 [T]."""
+    _need(topk_idx, torch.int32, "topk_idx", 2)
+    _need(query_start_loc, torch.int32, "query_start_loc", 1)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(gather_lens, torch.int32, "gather_lens", 1)
+    _need(combined, torch.int32, "combined", 2)
+    _need(combined_lens, torch.int32, "combined_lens", 1)
+    T, K = topk_idx.shape
+    return load_library().dsv4_combine_topk_swa_indices_compressed(
+        _ptr(topk_idx) if K > 0 else None, max(topk_idx.stride(0), K), K, _ptr(query_start_loc), _ptr(seq_lens),
+        _ptr(gather_lens), query_start_loc.numel() - 1, T, int(region_stride), int(compressed_len), int(top_k),
+        int(compress_ratio), int(window), _ptr(combined), max(combined.stride(0), combined.shape[1]),
+        combined.shape[1], _ptr(combined_lens), _stream(stream))
 
 
 def dsv4_sparse_mla_decode_workspace_size(num_tokens: int, num_heads: int, topk_width: int, window: int) -> int:

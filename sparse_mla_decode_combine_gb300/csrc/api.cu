@@ -206,6 +206,36 @@ extern "C" DSV4_API dsv4_status dsv4_combine_topk_swa_indices(const int32_t *top
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
+extern "C" DSV4_API dsv4_status dsv4_combine_topk_swa_indices_compressed(
+    const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width, const int32_t *query_start_loc,
+    const int32_t *seq_lens, const int32_t *gather_lens, int32_t num_reqs, int32_t num_tokens, int32_t region_stride,
+    int32_t compressed_len, int32_t top_k, int32_t compress_ratio, int32_t window, int32_t *combined,
+    int64_t combined_stride, int32_t combined_width, int32_t *combined_lens, dsv4_stream_t stream)
+{
+    if (num_reqs < 0 || num_tokens < 0 || topk_width < 0 || top_k < 0 || top_k > topk_width || compress_ratio < 1 ||
+        window < 0 || window > kMaxWindow || region_stride < 0 || compressed_len < 0)
+        return DSV4_ERR_INVALID_ARG;
+    if (topk_width > kMaxTopkWidth)
+        return DSV4_ERR_UNSUPPORTED;
+    if ((long long)region_stride * num_reqs > INT_MAX || (long long)combined_width < (long long)top_k + window)
+        return DSV4_ERR_INVALID_ARG;
+    if (num_reqs == 0 || num_tokens == 0)
+        return DSV4_OK;
+    if (query_start_loc == nullptr || seq_lens == nullptr || gather_lens == nullptr || combined == nullptr ||
+        combined_lens == nullptr || combined_stride < combined_width)
+        return DSV4_ERR_INVALID_ARG;
+    if (top_k > 0 && (topk_idx == nullptr || topk_stride < topk_width))
+        return DSV4_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    if (device_info(&status, nullptr) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    cudaError_t e = launch_combine_compressed(topk_idx, topk_stride, query_start_loc, seq_lens, gather_lens, num_reqs,
+                                              num_tokens, region_stride, compressed_len, top_k, compress_ratio, window,
+                                              combined, combined_stride, combined_width, combined_lens, status,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
 extern "C" DSV4_API size_t dsv4_sparse_mla_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk_width,
                                                         int32_t window)
 {

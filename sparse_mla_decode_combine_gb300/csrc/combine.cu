@@ -136,7 +136,102 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t *__rest
         combined_lens[t] = total + swa;
 }
 
+// Compressed-region combine (the page's full variant): one CTA per token row.  The CTA finds
+// the request whose query range holds its row (a parallel search over query_start_loc), then
+// writes the row one entry per thread at a time (coalesced top-k reads and row writes).  A row
+// that no request covers is written as -1 with length 0 and flags the bad-index status.
+constexpr int kCompThreads = 256;
+
+constexpr int kCompRun = 4;   // entries per thread per pass: one 16-byte store when the row is aligned
+
+__global__ void __launch_bounds__(kCompThreads) combine_compressed_kernel(
+    const int32_t *__restrict__ topk, int64_t topk_stride, const int32_t *__restrict__ qsl,
+    const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ gather_lens, int num_reqs, int region_stride,
+    int compressed_len, int top_k, int compress_ratio, int window, int32_t *__restrict__ combined,
+    int64_t combined_stride, int combined_width, int32_t *__restrict__ combined_lens, unsigned *status)
+{
+    __shared__ int req;
+    const long long t = blockIdx.x;
+    const int32_t *in = topk + t * topk_stride;
+    // the first pass's top-k entries do not depend on the request: their loads go out first
+    int x0[kCompRun];
+#pragma unroll
+    for (int u = 0; u < kCompRun; ++u) {
+        const int k = kCompRun * threadIdx.x + u;
+        x0[u] = k < top_k ? __ldg(in + k) : -1;
+    }
+    const long long base = qsl[0];
+    if (threadIdx.x == 0)
+        req = -1;
+    __syncthreads();
+    for (int b = threadIdx.x; b < num_reqs; b += kCompThreads)
+        if (qsl[b] - base <= t && t < qsl[b + 1] - base)
+            req = b;
+    __syncthreads();
+    const int b = req;
+    int32_t *row = combined + t * combined_stride;
+    const bool vec = (reinterpret_cast<uintptr_t>(row) % 16 == 0) && (combined_width % kCompRun == 0);
+    int tk = 0, sw = 0;
+    long long region = 0, win0 = 0;
+    if (b >= 0) {
+        // 64-bit intermediates, truncated to 32 bits on output (the page's arithmetic is 32-bit)
+        const long long qs = qsl[b] - base;
+        const long long qe = qsl[b + 1] - base;
+        const long long pos = (long long)seq_lens[b] - (qe - qs) + (t - qs);
+        const long long gather_start = (long long)seq_lens[b] - gather_lens[b];
+        region = (long long)region_stride * b;
+        if (pos + 1 > 0) {
+            tk = (int)min((pos + 1) / compress_ratio, (long long)top_k);
+            sw = (int)min(pos + 1, (long long)window);
+        }
+        win0 = region + compressed_len + (pos - sw + 1 - gather_start);
+    } else if (threadIdx.x == 0) {   // no request covers this row: -1, length 0
+        atomicOr(status, kStatusBadIndex);
+    }
+    auto entry = [&](int k, int x) -> int32_t {
+        if (k < tk)
+            return (x >= 0 && x < compressed_len) ? (int32_t)(region + x) : -1;
+        if (k < tk + sw)
+            return (int32_t)(win0 + (k - tk));
+        return -1;
+    };
+    for (int k0 = kCompRun * threadIdx.x; k0 < combined_width; k0 += kCompRun * kCompThreads) {
+        int32_t v[kCompRun];
+#pragma unroll
+        for (int u = 0; u < kCompRun; ++u) {
+            const int k = k0 + u;
+            const int x = k0 < kCompRun * kCompThreads ? x0[u] : (k < tk ? __ldg(in + k) : -1);
+            v[u] = entry(k, x);
+        }
+        if (vec) {
+            *reinterpret_cast<int4 *>(row + k0) = make_int4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < kCompRun; ++u)
+                if (k0 + u < combined_width)
+                    row[k0 + u] = v[u];
+        }
+    }
+    if (threadIdx.x == 0)
+        combined_lens[t] = tk + sw;
+}
+
 }  // namespace
+
+cudaError_t launch_combine_compressed(const int32_t *topk, int64_t topk_stride, const int32_t *qsl,
+                                      const int32_t *seq_lens, const int32_t *gather_lens, int num_reqs,
+                                      int num_tokens, int region_stride, int compressed_len, int top_k,
+                                      int compress_ratio, int window, int32_t *combined, int64_t combined_stride,
+                                      int combined_width, int32_t *combined_lens, unsigned *status,
+                                      cudaStream_t stream)
+{
+    if (num_reqs <= 0 || num_tokens <= 0)
+        return cudaSuccess;
+    combine_compressed_kernel<<<num_tokens, kCompThreads, 0, stream>>>(
+        topk, topk_stride, qsl, seq_lens, gather_lens, num_reqs, region_stride, compressed_len, top_k,
+        compress_ratio, window, combined, combined_stride, combined_width, combined_lens, status);
+    return cudaGetLastError();
+}
 
 int combine_table_bits(int topk_width)
 {

@@ -90,6 +90,13 @@ cudaError_t launch_combine(const int32_t *topk, int64_t topk_stride, int topk_wi
                            int64_t combined_stride, int combined_width, int32_t *combined_lens, int table_bits,
                            cudaStream_t stream);
 
+cudaError_t launch_combine_compressed(const int32_t *topk, int64_t topk_stride, const int32_t *qsl,
+                                      const int32_t *seq_lens, const int32_t *gather_lens, int num_reqs,
+                                      int num_tokens, int region_stride, int compressed_len, int top_k,
+                                      int compress_ratio, int window, int32_t *combined, int64_t combined_stride,
+                                      int combined_width, int32_t *combined_lens, unsigned *status,
+                                      cudaStream_t stream);
+
 // Launches `kernel(p)` so that it may start while the previous kernel in the stream
 // finishes (programmatic dependent launch); the kernel waits for that kernel's results
 // with griddepcontrol.wait before reading them.

@@ -53,6 +53,16 @@ def test_host_side_argument_errors(lib):
     assert lib.dsv4_combine_topk_swa_indices(None, 9000, 9000, None, None, 1, 0, None, 0, 9000, None, S) == pkg.DSV4_ERR_UNSUPPORTED
     assert lib.dsv4_combine_topk_swa_indices(None, 4, 4, None, ctypes.c_void_p(16), 1, 8, None, 12, 11, None, S) == pkg.DSV4_ERR_INVALID_ARG
     assert lib.dsv4_combine_topk_swa_indices(None, 4, 4, None, None, 0, 8, None, 12, 12, None, S) == pkg.DSV4_OK
+    # compressed combine: top_k above the row width, ratio 0, too narrow output, region overflow, nothing to do
+    P = ctypes.c_void_p(16)
+    cc = lib.dsv4_combine_topk_swa_indices_compressed
+    #        topk, stride, width, qsl, seq, gather, R, T, M,  N,  top_k, C, W, combined, cstride, cwidth, lens, stream
+    assert cc(P, 4, 4, P, P, P, 1, 1, 64, 8, 5, 1, 0, P, 8, 8, P, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert cc(P, 4, 4, P, P, P, 1, 1, 64, 8, 4, 0, 0, P, 8, 8, P, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert cc(P, 4, 4, P, P, P, 1, 1, 64, 8, 4, 1, 8, P, 11, 11, P, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert cc(P, 4, 4, P, P, P, 3, 1, 1 << 30, 8, 4, 1, 0, P, 8, 8, P, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert cc(P, 9000, 9000, P, P, P, 1, 1, 64, 8, 4, 1, 0, P, 8, 8, P, S) == pkg.DSV4_ERR_UNSUPPORTED
+    assert cc(None, 4, 4, None, None, None, 0, 0, 64, 8, 4, 1, 4, None, 8, 8, None, S) == pkg.DSV4_OK
     # decode: unsupported head count, non-finite scale, missing pointers
     args = [None, 576 * 16, None, 1, 64, None, 1, 1, 1, None, None, 0, 0, None, ctypes.c_void_p(16), 1, 16, 8, None,
             1.0, None, None, None, 0, S]
