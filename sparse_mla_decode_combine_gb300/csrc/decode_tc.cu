@@ -449,11 +449,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const bool is_mma = warp == 0;
     const int wid = tid - 32;            // worker index 0..511 (warps 1-16)
 
-    // every input may come from the previous kernel in the stream; the next kernel may be
-    // scheduled now (it waits for this grid's results itself)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
     // ---- shared memory carve-up (1024-byte aligned base for the swizzled tiles)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -475,6 +470,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small + kOffTmem);
     volatile int *flags = reinterpret_cast<volatile int *>(small + kOffFlags);   // [0] abort, [1] rescale block tag
     int *hkey = reinterpret_cast<int *>(gbase + kQBytes);          // combine hash set (K tile region)
+
+    // ---- set-up that reads no input, ahead of the wait for the previous grid: barriers, TMEM,
+    // the combine's empty hash set
+    if (tid == 0) {
+        mbar_init(bar_s, 1);
+        mbar_init(bar_p, kWorkers / 32);
+        for (int m = 0; m < 4; ++m)
+            mbar_init(bar_pv + 8 * m, 1);
+        for (int g = 0; g < kGroups; ++g)
+            mbar_init(bar_grp + 8 * g, kWorkers / 32);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        flags[0] = 0;
+        flags[1] = 0;
+    }
+    if (is_mma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    const int bits = p.table_bits;
+    const int table = 1 << bits;
+    int *hmin = hkey + table;
+    for (int i = tid; i < table; i += kThreads) {
+        hkey[i] = -1;
+        hmin[i] = INT_MAX;
+    }
+    if (tid < kHeadSlots)
+        slots[tid] = -1;
+    tc_before();
+
+    // every input may come from the previous kernel in the stream; the next kernel may be
+    // scheduled now (it waits for this grid's results itself)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- early loads: the token's sizes and top-k run first (the combine waits on them), then Q
     const int seq_len = p.seq_lens[t];
@@ -517,15 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const long long lo = (long long)pos - p.window + 1;
     const int win_lo = lo < 0 ? 0 : (int)lo;
     const int swa = seq_len > 0 ? pos - win_lo + 1 : 0;
-    const int bits = p.table_bits;
-    const int table = 1 << bits;
-    int *hmin = hkey + table;
-    for (int i = tid; i < table; i += kThreads) {
-        hkey[i] = -1;
-        hmin[i] = INT_MAX;
-    }
-    if (tid < kHeadSlots)
-        slots[tid] = -1;
     __syncthreads();
     // first occurrence of each position: the smallest top-k index holding it
     auto insert = [&](int v, int i) {
@@ -620,6 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     }
 
     if (nblocks == 0) {   // no key in this split
+        if (is_mma) {   // TMEM back (its address is visible after the combine's barriers)
+            tc_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot), "r"(kTmemCols)
+                         : "memory");
+        }
         if (p.splits == 1) {   // zero output, LSE from the sink alone
             if (tid < kNH && p.lse)
                 p.lse[(int64_t)t * p.num_heads + h0 + tid] = p.sink ? p.sink[h0 + tid] : -INFINITY;
@@ -651,23 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int rrow = 8 * (((warp - 1) - (lane >> 2)) & 15) + (lane >> 2);
     const float c2 = p.scale * 1.4426950408889634f;      // logits in log2 units per raw dot product
 
-    if (tid == 0) {
-        mbar_init(bar_s, 1);
-        mbar_init(bar_p, kWorkers / 32);
-        for (int m = 0; m < 4; ++m)
-            mbar_init(bar_pv + 8 * m, 1);
-        for (int g = 0; g < kGroups; ++g)
-            mbar_init(bar_grp + 8 * g, kWorkers / 32);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        flags[0] = 0;
-        flags[1] = 0;
-    }
-    if (is_mma) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    } else {   // Q -> swizzled K-major B operand
+    if (!is_mma) {   // Q -> swizzled K-major B operand
 #pragma unroll
         for (int j = 0; j < kQLoads; ++j) {
             const int i = wid + kWorkers * j;
