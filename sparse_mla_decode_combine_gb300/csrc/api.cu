@@ -107,7 +107,7 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
     }
     p.chunk = best_chunk;
     p.splits = std::max(1, (p.cw + p.chunk - 1) / p.chunk);
-    p.combine_table_bits = combine_table_bits(topk_width);
+    p.combine_table_bits = tc ? decode_tc_table_bits(topk_width) : combine_table_bits(topk_width);
 
     size_t off = 0;
     p.off_combined = off;

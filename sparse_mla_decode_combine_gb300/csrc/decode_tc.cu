@@ -93,7 +93,6 @@ constexpr int kSmemBytes = kQBytes + kKBytes + kSmallBytes + 1024;   // + alignm
 constexpr int kQLoads = kNH * (kDim / 8) / kWorkers;                 // 9 16-byte Q pieces per worker
 constexpr int kGroups = 2;               // S^T is issued in 2 groups: column chunks 0-5, then 6-8
 static_assert(kNH * (kDim / 8) % kWorkers == 0, "Q pieces per worker");
-static_assert(kKBytes >= 2 * (int)sizeof(int) * 2 * kMaxTopkWidth, "combine hash table fits the K tile");
 static_assert(kKBytes >= kNH * kLatent * (int)sizeof(float), "partial O fits the K tile");
 
 // instruction descriptors (kind::f16): D f32, A/B bf16, M = 128, N = 64
@@ -435,6 +434,28 @@ __device__ __forceinline__ int slot_of_position(const DecodeParams &p, int row, 
 
 __device__ __forceinline__ unsigned hash_pos(int v, int bits) { return ((unsigned)v * 0x9E3779B1u) >> (32 - bits); }
 
+constexpr int kHashBitsMax = 14;                       // 2^14 slots of 8 bytes: the K tile region before the block table
+constexpr unsigned long long kHashEmpty = ~0ull;
+static_assert((8 << kHashBitsMax) <= kBtOffset, "combine hash table fits before the block-table cache");
+
+// The slot of position v holds (v << 32) | smallest top-k index seen for v.  Returns the slot;
+// the first writer of a position claims the slot with one CAS, a repeat lowers the index.
+__device__ __forceinline__ unsigned hash_insert(unsigned long long *tab, int bits, int v, int i)
+{
+    const unsigned long long want = ((unsigned long long)(unsigned)v << 32) | (unsigned)i;
+    unsigned h = hash_pos(v, bits);
+    while (true) {
+        const unsigned long long prev = atomicCAS(&tab[h], kHashEmpty, want);
+        if (prev == kHashEmpty)
+            return h;
+        if ((unsigned)(prev >> 32) == (unsigned)v) {
+            atomicMin(&tab[h], want);
+            return h;
+        }
+        h = (h + 1u) & ((1u << bits) - 1u);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -490,13 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // (position, top-k index) pairs, 64 bits a slot, at most a quarter full
     const int bits = p.table_bits;
     const int table = 1 << bits;
-    int *hmin = hkey + table;
-    for (int i = tid; i < table; i += kThreads) {
-        hkey[i] = -1;
-        hmin[i] = INT_MAX;
-    }
+    unsigned long long *htab = reinterpret_cast<unsigned long long *>(hkey);
+    for (int i = tid; i < table; i += kThreads)
+        htab[i] = kHashEmpty;
     if (tid < kHeadSlots)
         slots[tid] = -1;
     tc_before();
@@ -548,28 +568,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int win_lo = lo < 0 ? 0 : (int)lo;
     const int swa = seq_len > 0 ? pos - win_lo + 1 : 0;
     __syncthreads();
-    // first occurrence of each position: the smallest top-k index holding it
-    auto insert = [&](int v, int i) {
-        unsigned h = hash_pos(v, bits);
-        while (true) {
-            const int prev = atomicCAS(&hkey[h], -1, v);
-            if (prev == -1 || prev == v) {
-                atomicMin(&hmin[h], i);
-                return;
-            }
-            h = (h + 1u) & (unsigned)(table - 1);
-        }
-    };
+    // first occurrence of each position: the smallest top-k index holding it; the entries of
+    // the first passes remember their slot
+    unsigned hs_slot[kPassLoads];
 #pragma unroll
     for (int u = 0; u < kPassLoads; ++u)
-        if (tv[u] >= 0 && tv[u] < win_lo)
-            insert(tv[u], u * kThreads + tid);
+        hs_slot[u] = (tv[u] >= 0 && tv[u] < win_lo) ? hash_insert(htab, bits, tv[u], u * kThreads + tid) : 0u;
 #pragma unroll 1
     for (int ps = kPassLoads; ps < npass; ++ps) {
         const int i = ps * kThreads + tid;
         const int v = i < n ? __ldg(trow + i) : -1;
         if (v >= 0 && v < win_lo)
-            insert(v, i);
+            hash_insert(htab, bits, v, i);
     }
     __syncthreads();
     // survivors in input order: ballots of up to four passes, one barrier, then every thread
@@ -593,10 +603,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             vg[u] = v;
             bool keep = false;
             if (v >= 0 && v < win_lo) {
-                unsigned h = hash_pos(v, bits);
-                while (hkey[h] != v)
-                    h = (h + 1u) & (unsigned)(table - 1);
-                keep = hmin[h] == i;
+                unsigned h;
+                if (pg == 0) {
+                    h = hs_slot[u];
+                } else {
+                    h = hash_pos(v, bits);
+                    while ((unsigned)(htab[h] >> 32) != (unsigned)v)
+                        h = (h + 1u) & (unsigned)(table - 1);
+                }
+                keep = (unsigned)htab[h] == (unsigned)i;
             }
             bal[u] = __ballot_sync(0xffffffffu, keep);
             if (lane == 0)
@@ -621,7 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                     slot_row[rank] = sl;
             }
         }
-        __syncthreads();   // wsum is rewritten by the next group of passes
+        if (pg + kPassLoads < npass)
+            __syncthreads();   // wsum is rewritten by the next group of passes
     }
 
     const int L = total + swa;
@@ -1066,12 +1082,20 @@ int decode_tc_resident_ctas(int splits)
     return n;
 }
 
+int decode_tc_table_bits(int topk_width)
+{
+    int bits = 6;
+    while (bits < kHashBitsMax && (1 << bits) < 4 * topk_width)
+        ++bits;
+    return bits;
+}
+
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
 {
     if (p.num_tokens <= 0)
         return cudaSuccess;
     if (p.heads_per_group != kNH || p.chunk <= 0 || p.splits < 1 || p.splits > kMaxSplits || p.topk_width < 0 ||
-        p.topk_width > kMaxTopkWidth || p.table_bits < 1 || (2 * sizeof(int) << p.table_bits) > (size_t)kKBytes)
+        p.topk_width > kMaxTopkWidth || p.table_bits < 1 || p.table_bits > kHashBitsMax)
         return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(decode_tc_kernel), kSmemBytes, kAttrTc);
     if (e != cudaSuccess)
