@@ -432,6 +432,21 @@ __device__ __forceinline__ int slot_of_position(const DecodeParams &p, int row, 
     return phys * p.page + (idx - blk * p.page);
 }
 
+// L2 prefetch of the cache entry of position idx (through the cached block-table row); no
+// status is recorded here, the combine resolves the same position again.
+__device__ __forceinline__ void prefetch_entry(const DecodeParams &p, int idx, const int *bt_s)
+{
+    const int blk = idx / p.page;
+    if (blk >= p.max_blocks)
+        return;
+    const int phys = bt_s[blk];
+    if (phys < 0 || phys >= p.num_blocks)
+        return;
+    const int64_t slot = (int64_t)phys * p.page + (idx - blk * p.page);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.kv + slot * kEntryBytes), "r"((uint32_t)kEntryBytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ unsigned hash_pos(int v, int bits) { return ((unsigned)v * 0x9E3779B1u) >> (32 - bits); }
 
 constexpr int kHashBitsMax = 14;                       // 2^14 slots of 8 bytes: the K tile region before the block table
@@ -582,10 +597,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             hash_insert(htab, bits, v, i);
     }
     __syncthreads();
-    // survivors in input order: ballots of up to four passes, one barrier, then every thread
-    // ranks its entries; the ones of this split resolve to cache slots
     const int kbeg = split * p.chunk;
     const int klim = kbeg + p.chunk;
+    // the first two blocks' entries start towards L2 now, while the combine finishes: the rank of
+    // an entry is taken as its input index (exact unless earlier entries are dropped), the window
+    // as following all n top-k entries
+    if (row_ok && bt_cached) {
+        const int plim = min(klim, kbeg + 2 * kBK);
+#pragma unroll
+        for (int u = 0; u < kPassLoads; ++u) {
+            const int i = u * kThreads + tid;
+            if (tv[u] >= 0 && tv[u] < win_lo && i >= kbeg && i < plim)
+                prefetch_entry(p, tv[u], bt_s);
+        }
+        for (int j = max(0, kbeg - n) + tid; j < swa && n + j < plim; j += kThreads)
+            prefetch_entry(p, win_lo + j, bt_s);
+    }
+    // survivors in input order: ballots of up to four passes, one barrier, then every thread
+    // ranks its entries; the ones of this split resolve to cache slots
     int32_t *slot_row = p.combined + (int64_t)t * p.cw;   // cache slots of blocks >= 2 of this split
     int total = 0;
 #pragma unroll 1
