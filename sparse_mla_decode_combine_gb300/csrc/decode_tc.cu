@@ -939,8 +939,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
 
         if (quad == 0 && lane < 16)
             mrun[hs + lane] = m_run;
-        mbar_wait(bar_pv + 24, (uint32_t)((nblocks - 1) & 1), flags, p.status);
-        tc_after();
         float *rede = red + (nblocks & 1) * 4 * kNH;   // the buffer the last block did not use
 
         // ---- epilogue: row sums across the 128 lanes, then the normalised output or the staged partial
@@ -1009,6 +1007,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             }
         }
         named_bar(1, kWorkers);
+        // the row sums and statistics above only read this warp's own TMEM stores: they overlap
+        // the last block's P.V products, which the output needs
+        mbar_wait(bar_pv + 24, (uint32_t)((nblocks - 1) & 1), flags, p.status);
+        tc_after();
         if (p.splits == 1) {
             uint32_t x[16];
 #pragma unroll 1
