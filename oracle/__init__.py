@@ -8,6 +8,8 @@ Each function restates one step of the path (oracle.c names the page and
 section each follows):
   * ``e4m3_to_f64`` / ``ue8m0_to_f64`` / ``bf16_to_f64`` / ``dequant_entry`` - the cache format,
   * ``combine`` - top-k + sliding-window index combine with dedup and compaction,
+  * ``combine_compressed`` - the compressed-region variant of the combine,
+  * ``topk_select`` - top-k selection from indexer scores (what produces the top-k rows),
   * ``attend`` - sink-softmax MQA attention of one head over explicit keys,
   * ``merge`` - log-sum-exp merge of partial results over disjoint key sets,
   * ``sparse_mla_decode`` - the whole decode for all (or a subset of) tokens.
@@ -73,6 +75,8 @@ class Oracle:
         lib.oracle_combine.argtypes = [P, i64, i32, P, P, i32, i32, P, i64, i32, P]
         lib.oracle_combine_compressed.restype = ctypes.c_int
         lib.oracle_combine_compressed.argtypes = [P, i64, i32, P, P, P, i32, i32, i32, i32, i32, i32, P, i64, i32, P]
+        lib.oracle_topk_select.restype = ctypes.c_int
+        lib.oracle_topk_select.argtypes = [P, i64, i32, P, i32, i32, P, i64, P]
         lib.oracle_attend.restype = None
         lib.oracle_attend.argtypes = [P, P, i32, f64, ctypes.c_int, f64, P, P]
         lib.oracle_merge.restype = None
@@ -126,6 +130,18 @@ class Oracle:
                                                 _ptr(out), combined_width, combined_width, _ptr(lens))
         if rc != 0:
             raise ValueError("arguments outside the compressed combine's rules")
+        return out, lens
+
+    def topk_select(self, scores, num_cand, top_k: int):
+        """Top-k selection -> (topk_idx int32 [T, K] ascending then -1, topk_lens int32 [T])."""
+        sc = _c(scores, np.float32)
+        T, width = sc.shape
+        out = np.empty((T, top_k), dtype=np.int32)
+        lens = np.empty(T, dtype=np.int32)
+        rc = self.lib.oracle_topk_select(_ptr(sc), width, width, _ptr(_c(num_cand, np.int32)), T, int(top_k),
+                                         _ptr(out), top_k, _ptr(lens))
+        if rc != 0:
+            raise ValueError("top_k must be at least 1")
         return out, lens
 
     def attend(self, q, keys, softmax_scale: float, sink: Optional[float] = None):
@@ -211,6 +227,10 @@ def combine_compressed(topk_idx, query_start_loc, seq_lens, gather_lens, region_
                        compress_ratio, window, combined_width):
     return default().combine_compressed(topk_idx, query_start_loc, seq_lens, gather_lens, region_stride,
                                         compressed_len, top_k, compress_ratio, window, combined_width)
+
+
+def topk_select(scores, num_cand, top_k):
+    return default().topk_select(scores, num_cand, top_k)
 
 
 def attend(q, keys, softmax_scale, sink=None):

@@ -29,6 +29,9 @@
  *    definition: s_j = scale * q . k_j over 576 dims; with an optional sink
  *    logit sigma (in the same units as s), Z = sum_j e^{s_j} + e^{sigma},
  *    lse = ln Z, out = sum_j e^{s_j - lse} v_j.
+ *  - top-k selection from indexer scores (what produces topk_idx): "[Model] DeepSeek V4"
+ *    (vllm #40860), 实现拆解 2; the selection rule is written out with its readings at
+ *    oracle_topk_select.
  *  - merge of split partial results: the log-sum-exp combination, written out
  *    from its definition (not on the pages; needed when one token's keys are
  *    split over several workers).
@@ -150,6 +153,69 @@ int oracle_combine_compressed(const int32_t *topk_idx, int64_t topk_stride, int3
                 row[k] = -1;
             combined_lens[t] = (int32_t)(tk + sw);
         }
+    }
+    return 0;
+}
+
+/* Top-k selection from indexer scores: the step that produces topk_idx ("[Model] DeepSeek V4"
+ * (vllm #40860), 实现拆解 2: the MLA wrapper runs the Indexer ahead of the sparse attention).
+ * The pages print no selection rule; this is the plain definition, with these readings: row t's
+ * candidates are positions [0, n), n = num_cand[t] clamped to [0, width]; the selected set is
+ * the min(K, n) candidates that come first in the total order "larger score first, then smaller
+ * position", where -0 equals +0 and a NaN score ranks below every number; the output row holds
+ * the selected positions in ascending order, then -1; topk_lens[t] = min(K, n).
+ * Returns 0, or 1 for K < 1. */
+struct topk_item {
+    double v;      /* the score (0 for NaN) */
+    int nan;       /* 1 for a NaN score */
+    int32_t pos;
+};
+
+static int topk_before(const void *pa, const void *pb)
+{
+    const struct topk_item *a = pa, *b = pb;
+    if (a->nan != b->nan)
+        return a->nan ? 1 : -1;                           /* NaN after every number */
+    if (!a->nan && a->v != b->v)
+        return a->v > b->v ? -1 : 1;                      /* larger score first */
+    return a->pos < b->pos ? -1 : (a->pos > b->pos);      /* then the smaller position */
+}
+
+static int ascending_i32(const void *pa, const void *pb)
+{
+    const int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return a < b ? -1 : (a > b);
+}
+
+int oracle_topk_select(const float *scores, int64_t score_stride, int32_t width, const int32_t *num_cand,
+                       int32_t num_tokens, int32_t top_k, int32_t *topk_idx, int64_t topk_stride,
+                       int32_t *topk_lens)
+{
+    if (top_k < 1)
+        return 1;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int64_t n = num_cand[t];
+        if (n < 0)
+            n = 0;
+        if (n > width)
+            n = width;
+        struct topk_item *items = malloc(sizeof(struct topk_item) * (size_t)(n > 0 ? n : 1));
+        for (int64_t p = 0; p < n; ++p) {
+            const float x = scores[t * score_stride + p];
+            items[p].nan = isnan(x) ? 1 : 0;
+            items[p].v = items[p].nan ? 0.0 : (double)x + 0.0;   /* + 0.0 turns -0 into +0 */
+            items[p].pos = (int32_t)p;
+        }
+        qsort(items, (size_t)n, sizeof(struct topk_item), topk_before);
+        const int64_t m = n < top_k ? n : top_k;
+        int32_t *row = topk_idx + t * topk_stride;
+        for (int64_t k = 0; k < m; ++k)
+            row[k] = items[k].pos;
+        qsort(row, (size_t)m, sizeof(int32_t), ascending_i32);
+        for (int64_t k = m; k < top_k; ++k)
+            row[k] = -1;
+        topk_lens[t] = (int32_t)m;
+        free(items);
     }
     return 0;
 }

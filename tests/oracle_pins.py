@@ -384,6 +384,7 @@ def check_topk_lens_truncation(orc):
 # ----------------------------------------------------------------------------
 GOLDEN_COMPRESSED = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
                                  "combine_compressed_worked_examples.txt")
+GOLDEN_TOPK = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "topk_select_worked_examples.txt")
 
 
 def load_golden_compressed():
@@ -456,8 +457,87 @@ def check_combine_compressed_invariants(orc):
                 t += 1
 
 
+def load_golden_topk():
+    examples, cur = [], None
+    with open(GOLDEN_TOPK) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            if key == "example":
+                cur = dict(name=rest, rows=[])
+            elif key == "params":
+                cur["K"], cur["width"] = [int(v) for v in rest.split()]
+            elif key == "row":
+                nc, sc, want, ln = [p.strip() for p in rest.split("|")]
+                cur["rows"].append((int(nc), [float(v) for v in sc.split()], [int(v) for v in want.split()], int(ln)))
+            elif key == "end":
+                examples.append(cur)
+    return examples
+
+
+def check_topk_golden(orc):
+    for ex in load_golden_topk():
+        sc = np.array([r[1] for r in ex["rows"]], dtype=np.float32)
+        assert sc.shape[1] == ex["width"], ex["name"]
+        idx, ln = orc.topk_select(sc, [r[0] for r in ex["rows"]], ex["K"])
+        for i, (_, _, want, wl) in enumerate(ex["rows"]):
+            assert idx[i].tolist() == want, (ex["name"], i, idx[i].tolist(), want)
+            assert int(ln[i]) == wl, (ex["name"], i)
+
+
+def check_topk_distinct_vs_argpartition(orc):
+    """Distinct scores: the selected set is numpy's argpartition of the candidates."""
+    rng = np.random.default_rng(41)
+    for _ in range(40):
+        width = int(rng.integers(1, 400))
+        T = int(rng.integers(1, 5))
+        K = int(rng.integers(1, 300))
+        sc = np.stack([rng.permutation(width).astype(np.float32) * np.float32(rng.choice([-1.5, 0.25, 3.0]))
+                       + np.float32(rng.normal()) for _ in range(T)])
+        nc = rng.integers(-3, width + 5, size=T).astype(np.int32)
+        idx, ln = orc.topk_select(sc, nc, K)
+        for t in range(T):
+            n = int(min(max(nc[t], 0), width))
+            m = min(K, n)
+            want = np.sort(np.argpartition(-sc[t, :n].astype(np.float64), m - 1)[:m]) if m > 0 else np.zeros(0, int)
+            assert idx[t, :m].tolist() == want.tolist()
+            assert np.all(idx[t, m:] == -1) and int(ln[t]) == m
+
+
+def check_topk_invariants(orc):
+    """Tie-heavy rows with signed zeros, infinities and NaN: the row is ascending and -1 padded,
+    its length is min(K, n), and no candidate left out precedes a selected one in the order
+    (score, with -0 == +0 and NaN lowest; then position)."""
+    rng = np.random.default_rng(43)
+    pool = np.array([0.0, -0.0, 1.0, -1.0, 2.5, np.inf, -np.inf, np.nan, 7.0], dtype=np.float32)
+    for _ in range(60):
+        width = int(rng.integers(1, 120))
+        T = int(rng.integers(1, 4))
+        K = int(rng.integers(1, 60))
+        sc = rng.choice(pool, size=(T, width)).astype(np.float32)
+        nc = rng.integers(0, width + 3, size=T).astype(np.int32)
+        idx, ln = orc.topk_select(sc, nc, K)
+        for t in range(T):
+            n = int(min(nc[t], width))
+            m = min(K, n)
+            sel = idx[t, :m].tolist()
+            assert int(ln[t]) == m and np.all(idx[t, m:] == -1)
+            assert sel == sorted(set(sel)) and all(0 <= p < n for p in sel)
+
+            def rank(p):   # smaller = earlier in the order
+                x = float(sc[t, p])
+                return (1, 0.0, p) if np.isnan(x) else (0, -x, p)
+            if 0 < m < n:
+                worst_in = max(rank(p) for p in sel)
+                best_out = min(rank(p) for p in range(n) if p not in set(sel))
+                assert worst_in < best_out, (t, worst_in, best_out)
+
+
 ALL_CHECKS = [check_e4m3_codes, check_ue8m0, check_bf16, check_entry_layout, check_quantize_roundtrip,
               check_combine_golden, check_combine_bruteforce, check_combine_config1_lengths,
               check_dense_equivalence, check_order_padding_invariance, check_page_permutation, check_closed_forms,
               check_lse_identity_and_sink_limit, check_merge_partition, check_empty_and_bad_index,
-              check_topk_lens_truncation, check_combine_compressed_golden, check_combine_compressed_invariants]
+              check_topk_lens_truncation, check_combine_compressed_golden, check_combine_compressed_invariants,
+              check_topk_golden, check_topk_distinct_vs_argpartition, check_topk_invariants]

@@ -48,6 +48,17 @@ MUTANTS = [
      "(int32_t)(region + (pos - sw + 1 - gather_start) + j)"),
     ("compressed: invalid top-k compacted", "row[k] = (v >= 0 && v < compressed_len) ? (int32_t)(region + v) : -1;",
      "row[k] = (v >= 0 && v <= compressed_len) ? (int32_t)(region + v) : -1;"),
+    ("top-k: ties to the larger position", "return a->pos < b->pos ? -1 : (a->pos > b->pos);      /* then the smaller position */",
+     "return a->pos > b->pos ? -1 : (a->pos < b->pos);"),
+    ("top-k: NaN ranked first", "return a->nan ? 1 : -1;                           /* NaN after every number */",
+     "return a->nan ? -1 : 1;"),
+    ("top-k: smaller scores first", "return a->v > b->v ? -1 : 1;                      /* larger score first */",
+     "return a->v < b->v ? -1 : 1;"),
+    ("top-k: one candidate too many", "int64_t n = num_cand[t];", "int64_t n = num_cand[t] + 1;"),
+    ("top-k: selection order kept", "qsort(row, (size_t)m, sizeof(int32_t), ascending_i32);", ""),
+    ("top-k: -0 below +0", "items[p].v = items[p].nan ? 0.0 : (double)x + 0.0;",
+     "items[p].v = items[p].nan ? 0.0 : (signbit(x) && x == 0.0f ? -1e-300 : (double)x);"),
+    ("top-k: length not capped by K", "topk_lens[t] = (int32_t)m;", "topk_lens[t] = (int32_t)n;"),
 ]
 
 
