@@ -60,8 +60,10 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["decode", "combine-compressed"], default="decode",
-                    help="decode (the headline) or the compressed-region combine on its own")
+    ap.add_argument("--op", choices=["decode", "combine-compressed", "topk-select"], default="decode",
+                    help="decode (the headline), or the compressed-region combine or the top-k selection on its own")
+    ap.add_argument("--topk-workload", choices=["long-batch", "long-decode"], default="long-batch",
+                    help="top-k selection workload (synth.topk_config)")
     ap.add_argument("--replicas", type=int, default=0,
                     help="workload replicas to rotate through (default: enough for 4x the L2)")
     return ap.parse_args()
@@ -584,8 +586,94 @@ def run_combine_compressed(args):
     return 0
 
 
+def run_topk_select(args):
+    """Top-k selection on its own (synth.topk_config): bytes per step are the candidate scores
+    read once (4 * sum n_t) plus the rows and lengths written (T * (4 * K + 4))."""
+    import torch
+    import synth
+    import sparse_mla_decode_combine_gb300 as pkg
+    from sparse_mla_decode_combine_gb300 import build as pkg_build
+    pkg_build.build()
+    pkg.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = synth.topk_config(args.topk_workload)
+    T, K = w.num_tokens, w.top_k
+    nc = np.clip(w.num_cand, 0, w.width).astype(np.int64)
+    bytes_per_step = int(4 * nc.sum() + T * (4 * K + 4))
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    reps = args.replicas if args.replicas > 0 else max(2, math.ceil(4 * l2 / (4 * int(nc.sum()))))
+    base = torch.from_numpy(w.scores).to(dev)
+    scs = [base.clone() for _ in range(reps)]
+    del base
+    nc_d = torch.from_numpy(w.num_cand).to(dev)
+    outs = [torch.empty((T, K), dtype=torch.int32, device=dev) for _ in range(reps)]
+    lens = [torch.empty((T,), dtype=torch.int32, device=dev) for _ in range(reps)]
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        pkg.check(pkg.dsv4_topk_select(scs[i % reps], nc_d, K, outs[i % reps], lens[i % reps], stream=stream))
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            step(i)
+    torch.cuda.synchronize()
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        return g
+    graph = capture(reps)
+    replays, rem = divmod(max(args.steps, 1), reps)
+    tail = capture(rem) if rem else None
+    torch.cuda.synchronize()
+    steps = replays * reps + rem
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    sampler.start()
+    time.sleep(0.2)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        if tail is not None:
+            tail.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    step_s = ms / 1e3 / steps
+    hbm_peak, _, _, peak_src = peaks()
+    ach = bytes_per_step / step_s / 1e9
+    desc = {"long-batch": "top-k selection: 128 tokens x 32768 candidate scores, top-k 2048",
+            "long-decode": "top-k selection: 16 tokens x 1024..131071 candidate scores, top-k 2048"}[w.name]
+    line = {"metric": "top-k selection query-tokens/s (bytes moved vs HBM roofline)",
+            "value": T / step_s, "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": desc, "tokens_per_step": T, "candidates_per_step": int(nc.sum()), "top_k": K,
+                       "replicas": reps, "l2": f"inputs larger than L2: {reps} rotating replicas"},
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                         "traffic": None, "kernel": "topk_select_kernel",
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+                         "algorithmic_bytes_per_launch": bytes_per_step,
+                         "timed": "one call (one launch) per step, CUDA events on the launching stream"},
+            "gpu_launches": steps, "launches_per_step": 1, "clocks": sampler.summary(t0, t1)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.op == "topk-select":
+        if args.impl == "reference" or int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        return run_topk_select(args)
     if args.op == "combine-compressed":
         if args.impl == "reference" or int(os.environ.get("RANK", "0")) != 0:
             return 0

@@ -154,6 +154,35 @@ DSV4_API dsv4_status dsv4_combine_topk_swa_indices_compressed(
     int64_t combined_stride, int32_t combined_width, int32_t *combined_lens, dsv4_stream_t stream);
 
 /*
+ * dsv4_topk_select -- each token's top-k row from its indexer scores (the step that produces
+ * topk_idx for the decode).
+ *
+ * Source: vllm #40860 "[Model] DeepSeek V4", section 实现拆解 2 (the MLA wrapper runs the
+ * Indexer ahead of the sparse attention).  The pages print no selection rule; this is the
+ * plain definition.  Token t's candidates are positions [0, n), n = num_cand[t] clamped to
+ * [0, score_width]; the selected set is the min(top_k, n) candidates that come first in the
+ * order "larger score first, then the smaller position", where -0 equals +0 and a NaN score
+ * ranks below every number.
+ *   topk_idx[t][0 .. m)        the selected positions in ascending order, m = min(top_k, n)
+ *   topk_idx[t][m .. top_k)    -1
+ *   topk_lens[t]               m
+ *
+ * Arguments:
+ *   scores       fp32 [num_tokens, score_width], row stride score_stride (>= score_width).
+ *   num_cand     int32 [num_tokens]: candidates per token (a decode token at position pos
+ *                has pos + 1 raw positions, or (pos + 1) / ratio compressed entries).
+ *   num_tokens   >= 0 (0 enqueues nothing); top_k >= 1.
+ *   topk_idx     int32 [num_tokens, top_k], row stride topk_stride (>= top_k).
+ *   topk_lens    int32 [num_tokens], or NULL.
+ * All buffers are device memory owned by the caller; nothing is allocated.  The scores are
+ * read from HBM once and up to four more times from L2 (the histogram rounds and the final
+ * pass).  Returns DSV4_OK, DSV4_ERR_INVALID_ARG or DSV4_ERR_CUDA.
+ */
+DSV4_API dsv4_status dsv4_topk_select(const float *scores, int64_t score_stride, int32_t score_width,
+                                      const int32_t *num_cand, int32_t num_tokens, int32_t top_k, int32_t *topk_idx,
+                                      int64_t topk_stride, int32_t *topk_lens, dsv4_stream_t stream);
+
+/*
  * dsv4_sparse_mla_decode_workspace_size -- bytes of device workspace dsv4_sparse_mla_decode needs.
  *
  * The size depends on the arguments and on the multiprocessor count of the current

@@ -29,7 +29,7 @@ DSV4_ERR_UNSUPPORTED = 5
 STATUS_NAMES = {0: "DSV4_OK", 1: "DSV4_ERR_INVALID_ARG", 2: "DSV4_ERR_BAD_INDEX", 3: "DSV4_ERR_TIMEOUT",
                 4: "DSV4_ERR_CUDA", 5: "DSV4_ERR_UNSUPPORTED"}
 
-EXPORTED = ("dsv4_combine_topk_swa_indices", "dsv4_combine_topk_swa_indices_compressed",
+EXPORTED = ("dsv4_combine_topk_swa_indices", "dsv4_combine_topk_swa_indices_compressed", "dsv4_topk_select",
             "dsv4_sparse_mla_decode_workspace_size", "dsv4_sparse_mla_decode", "dsv4_sparse_mla_decode_noalloc",
             "dsv4_get_device_status")
 
@@ -67,6 +67,8 @@ def load_library():
     lib.dsv4_combine_topk_swa_indices_compressed.restype = ctypes.c_int
     lib.dsv4_combine_topk_swa_indices_compressed.argtypes = [P, i64, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                              P, i64, i32, P, P]
+    lib.dsv4_topk_select.restype = ctypes.c_int
+    lib.dsv4_topk_select.argtypes = [P, i64, i32, P, i32, i32, P, i64, P, P]
     lib.dsv4_sparse_mla_decode_workspace_size.restype = ctypes.c_size_t
     lib.dsv4_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.dsv4_sparse_mla_decode.restype = ctypes.c_int
@@ -139,6 +141,21 @@ def dsv4_combine_topk_swa_indices_compressed(topk_idx: torch.Tensor, query_start
         _ptr(gather_lens), query_start_loc.numel() - 1, T, int(region_stride), int(compressed_len), int(top_k),
         int(compress_ratio), int(window), _ptr(combined), max(combined.stride(0), combined.shape[1]),
         combined.shape[1], _ptr(combined_lens), _stream(stream))
+
+
+def dsv4_topk_select(scores: torch.Tensor, num_cand: torch.Tensor, top_k: int, topk_idx: torch.Tensor,
+                     topk_lens: Optional[torch.Tensor] = None, stream=None) -> int:
+    """scores float32 [T, width] (unit stride along a row); num_cand int32 [T];
+    topk_idx int32 [T, top_k]; topk_lens int32 [T] or None."""
+    _need(scores, torch.float32, "scores", 2)
+    _need(num_cand, torch.int32, "num_cand", 1)
+    _need(topk_idx, torch.int32, "topk_idx", 2)
+    _need(topk_lens, torch.int32, "topk_lens", 1)
+    T, width = scores.shape
+    return load_library().dsv4_topk_select(
+        _ptr(scores) if width > 0 else None, max(scores.stride(0), width), width, _ptr(num_cand), T, int(top_k),
+        _ptr(topk_idx), max(topk_idx.stride(0), topk_idx.shape[1]), _ptr(topk_lens) if topk_lens is not None else None,
+        _stream(stream))
 
 
 def dsv4_sparse_mla_decode_workspace_size(num_tokens: int, num_heads: int, topk_width: int, window: int) -> int:

@@ -236,6 +236,27 @@ extern "C" DSV4_API dsv4_status dsv4_combine_topk_swa_indices_compressed(
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
+extern "C" DSV4_API dsv4_status dsv4_topk_select(const float *scores, int64_t score_stride, int32_t score_width,
+                                                 const int32_t *num_cand, int32_t num_tokens, int32_t top_k,
+                                                 int32_t *topk_idx, int64_t topk_stride, int32_t *topk_lens,
+                                                 dsv4_stream_t stream)
+{
+    if (num_tokens < 0 || top_k < 1 || score_width < 0)
+        return DSV4_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return DSV4_OK;
+    if (num_cand == nullptr || topk_idx == nullptr || topk_stride < top_k ||
+        (score_width > 0 && (scores == nullptr || score_stride < score_width)))
+        return DSV4_ERR_INVALID_ARG;
+    int sms = 0;
+    if (device_info(nullptr, &sms) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    cudaError_t e = launch_topk_select(scores, score_stride, score_width, num_cand, num_tokens, top_k, topk_idx,
+                                       topk_stride, topk_lens, topk_cluster_size(num_tokens, score_width, sms),
+                                       reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
 extern "C" DSV4_API size_t dsv4_sparse_mla_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk_width,
                                                         int32_t window)
 {

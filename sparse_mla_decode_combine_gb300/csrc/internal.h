@@ -103,6 +103,12 @@ cudaError_t launch_combine_compressed(const int32_t *topk, int64_t topk_stride, 
 cudaError_t launch_after_previous(const void *kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
                                   const DecodeParams &p);
 
+// Top-k selection: CTAs per token row (a thread-block cluster when > 1), and the launch.
+int topk_cluster_size(int num_tokens, int width, int sms);
+cudaError_t launch_topk_select(const float *scores, int64_t score_stride, int width, const int32_t *num_cand,
+                               int num_tokens, int top_k, int32_t *out, int64_t out_stride, int32_t *lens,
+                               int cluster, cudaStream_t stream);
+
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);

@@ -328,3 +328,47 @@ def to_device(w: Workload, device="cuda") -> dict:
                 req_idx=t(w.req_idx, torch.int32), topk_idx=t(w.topk_idx, torch.int32),
                 topk_lens=t(w.topk_lens, torch.int32), seq_lens=t(w.seq_lens, torch.int32),
                 window=int(w.window), sink=t(w.sink, torch.float32), softmax_scale=float(w.softmax_scale))
+
+
+# ----------------------------------------------------------------------------
+# indexer scores (inputs of the top-k selection)
+# ----------------------------------------------------------------------------
+@dataclasses.dataclass
+class TopkWorkload:
+    name: str
+    scores: np.ndarray       # float32 [T, width]
+    num_cand: np.ndarray     # int32 [T]
+    top_k: int
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.scores.shape[0])
+
+    @property
+    def width(self) -> int:
+        return int(self.scores.shape[1])
+
+
+def indexer_scores(rng, num_tokens: int, width: int) -> np.ndarray:
+    """float32 [T, width] indexer-like scores: ReLU of N(0, 1) draws rounded to BF16, so about
+    half the scores are exactly zero and equal scores are common among the rest."""
+    x = np.maximum(rng.standard_normal((num_tokens, width), dtype=np.float32), np.float32(0))
+    return (bf16_bits(x).astype(np.uint32) << 16).view(np.float32)
+
+
+def topk_config(name: str) -> TopkWorkload:
+    """Top-k selection workloads shaped like the decode workloads' top-k rows:
+      "long-batch"   128 tokens, 32768 candidates each, top-k 2048 (the long-context decode);
+      "long-decode"  16 tokens, 1024..131071 candidates (uniform), top-k 2048 (the very long
+                     decode: few rows, each split over a cluster of CTAs)."""
+    if name == "long-batch":
+        rng = np.random.default_rng(2003)
+        T, width = 128, 32768
+        nc = np.full(T, width, dtype=np.int32)
+    elif name == "long-decode":
+        rng = np.random.default_rng(2005)
+        T, width = 16, 131072
+        nc = rng.integers(1024, width, size=T).astype(np.int32)
+    else:
+        raise ValueError(name)
+    return TopkWorkload(name=name, scores=indexer_scores(rng, T, width), num_cand=nc, top_k=2048)

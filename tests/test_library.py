@@ -63,6 +63,16 @@ def test_host_side_argument_errors(lib):
     assert cc(P, 4, 4, P, P, P, 3, 1, 1 << 30, 8, 4, 1, 0, P, 8, 8, P, S) == pkg.DSV4_ERR_INVALID_ARG
     assert cc(P, 9000, 9000, P, P, P, 1, 1, 64, 8, 4, 1, 0, P, 8, 8, P, S) == pkg.DSV4_ERR_UNSUPPORTED
     assert cc(None, 4, 4, None, None, None, 0, 0, 64, 8, 4, 1, 4, None, 8, 8, None, S) == pkg.DSV4_OK
+    # top-k selection: K < 1, negative token count, missing pointers, narrow output rows, nothing to do
+    tk = lib.dsv4_topk_select
+    #        scores, stride, width, num_cand, T, K, idx, istride, lens, stream
+    assert tk(P, 16, 16, P, 1, 0, P, 4, None, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert tk(P, 16, 16, P, -1, 4, P, 4, None, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert tk(None, 16, 16, P, 1, 4, P, 4, None, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert tk(P, 16, 16, None, 1, 4, P, 4, None, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert tk(P, 16, 16, P, 1, 4, P, 3, None, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert tk(P, 8, 16, P, 1, 4, P, 4, None, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert tk(None, 0, 0, None, 0, 4, None, 0, None, S) == pkg.DSV4_OK
     # decode: unsupported head count, non-finite scale, missing pointers
     args = [None, 576 * 16, None, 1, 64, None, 1, 1, 1, None, None, 0, 0, None, ctypes.c_void_p(16), 1, 16, 8, None,
             1.0, None, None, None, 0, S]
