@@ -12,9 +12,11 @@
 // v* and how many keys equal to v* the selection takes.  Each round every CTA builds its
 // segment's histogram in shared memory, then reduces one slice of the bins across the
 // cluster through distributed shared memory; the owner of the slice holding the K-th key
-// broadcasts the digit.  A last pass over the row in position order writes every position
-// with key > v* and the first ones with key == v*.  The first pass reads the scores from
-// HBM; the later ones normally hit L2.
+// broadcasts the digit.  The first round reads the scores from HBM with 16-byte loads issued
+// four deep and keeps the segment's keys in shared memory (up to 40960 keys a CTA), so the
+// later rounds and the compaction read no global memory.  The compaction walks the segment
+// in position order, one contiguous chunk per warp with warp scans only, and writes every
+// position with key > v* and the first ones with key == v*.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,8 +28,8 @@ namespace {
 constexpr int kTkThreads = 512;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkBins = 2048;          // 11-bit digits
-constexpr int kTkItems = 8;            // final pass: consecutive positions per thread
-constexpr int kTkTile = kTkThreads * kTkItems;
+constexpr int kTkCacheKeys = 40960;    // keys of a segment kept in shared memory (160 KB)
+constexpr int kTkStep = 32 * 8;        // compaction: a warp takes 8 consecutive positions per lane
 
 struct TopkParams {
     const float *scores;
@@ -39,6 +41,7 @@ struct TopkParams {
     int64_t out_stride;
     int32_t *lens;
     int32_t cluster;
+    int32_t cache;   // 1: every segment's keys fit the shared-memory cache
 };
 
 // Order-preserving key: larger score -> larger key; -0 and +0 share a key; NaN -> 0, below
@@ -117,16 +120,104 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *wsum, uint3
     return r;
 }
 
+// Visits every key of the segment row[lo, hi): from the shared-memory cache (kc[i - lo]) when
+// `cached`, else from global memory, storing it into the cache when `fill`.  Loads are issued
+// four deep before any key is used.  f(key) must not synchronise.
+template <class F>
+__device__ __forceinline__ void visit_keys(const float *row, int64_t lo, int64_t hi, bool vec, uint32_t *kc,
+                                           bool cached, bool fill, F f)
+{
+    const int tid = threadIdx.x;
+    const int64_t len = hi - lo;
+    const int64_t n4 = len / 4;
+    if (cached) {
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(kc);
+        for (int64_t b = 0; b < n4; b += 4 * kTkThreads) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t i = b + j * kTkThreads + tid;
+                v[j] = i < n4 ? k4[i] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (b + j * kTkThreads + tid < n4) {
+                    f(v[j].x);
+                    f(v[j].y);
+                    f(v[j].z);
+                    f(v[j].w);
+                }
+        }
+        for (int64_t i = 4 * n4 + tid; i < len; i += kTkThreads)
+            f(kc[i]);
+        return;
+    }
+    if (vec) {
+        const float4 *r4 = reinterpret_cast<const float4 *>(row + lo);
+        for (int64_t b = 0; b < n4; b += 4 * kTkThreads) {
+            float4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t i = b + j * kTkThreads + tid;
+                v[j] = i < n4 ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t i = b + j * kTkThreads + tid;
+                if (i < n4) {
+                    const uint4 k = make_uint4(order_key(v[j].x), order_key(v[j].y), order_key(v[j].z),
+                                               order_key(v[j].w));
+                    if (fill)
+                        reinterpret_cast<uint4 *>(kc)[i] = k;
+                    f(k.x);
+                    f(k.y);
+                    f(k.z);
+                    f(k.w);
+                }
+            }
+        }
+    } else {
+        for (int64_t b = 0; b < 4 * n4; b += 4 * kTkThreads) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t i = b + j * kTkThreads + tid;
+                v[j] = i < 4 * n4 ? __ldg(row + lo + i) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t i = b + j * kTkThreads + tid;
+                if (i < 4 * n4) {
+                    const uint32_t k = order_key(v[j]);
+                    if (fill)
+                        kc[i] = k;
+                    f(k);
+                }
+            }
+        }
+    }
+    for (int64_t i = 4 * n4 + tid; i < len; i += kTkThreads) {
+        const uint32_t k = order_key(__ldg(row + lo + i));
+        if (fill)
+            kc[i] = k;
+        f(k);
+    }
+}
+
 __global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParams p)
 {
     __shared__ uint32_t hist[kTkBins];     // this CTA's histogram of the round
     __shared__ uint32_t slice[kTkBins];    // this CTA's slice of the cluster-wide histogram
     __shared__ uint32_t sums[8];           // slice totals of every CTA of the cluster
     __shared__ uint32_t bcast[2];          // the round's digit and remaining count
-    __shared__ uint32_t cnt[8][2];         // final pass: (> v*, == v*) counts per CTA
+    __shared__ uint32_t cnt[8][2];         // (> v*, == v*) counts per CTA
     __shared__ uint32_t wsum[kTkWarps];
+    __shared__ uint32_t wcnt[kTkWarps][2];   // compaction: (> v*, == v*) counts per warp chunk
+    extern __shared__ uint4 kcache4[];     // the segment's keys (when p.cache)
+    uint32_t *kc = reinterpret_cast<uint32_t *>(kcache4);
 
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     const int CL = p.cluster;
     const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
     // a word into the shared memory of CTA `r` of the cluster (plain store without a cluster)
@@ -135,6 +226,12 @@ __global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParam
             st_remote(remote_addr(local, (uint32_t)r), v);
         else
             *local = v;
+    };
+    auto sync_all = [&]() {
+        if (CL > 1)
+            cluster_barrier();
+        else
+            __syncthreads();
     };
     const int64_t t = blockIdx.x / CL;
     int64_t n = p.num_cand[t];
@@ -156,9 +253,12 @@ __global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParam
     const int64_t lo = min(n, (int64_t)rank * seg);
     const int64_t hi = min(n, lo + seg);
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    const bool cache = p.cache != 0;
 
-    // ---- three digit rounds: find the K-th largest key
+    // ---- three digit rounds find the K-th largest key v* and how many keys equal to it are
+    // taken (rem); this CTA's keys above v* (gt) and equal to it (eq) come from its histograms
     uint32_t prefix = 0u, pmask = 0u, rem = (uint32_t)m;
+    uint32_t gt_local = 0u, eq_local = 0u;
 #pragma unroll 1
     for (int round = 0; round < 3; ++round) {
         const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
@@ -167,43 +267,25 @@ __global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParam
         for (int i = tid; i < nb; i += kTkThreads)
             hist[i] = 0u;
         __syncthreads();
-        auto count = [&](float x) {
-            const uint32_t k = order_key(x);
+        visit_keys(row, lo, hi, vec, kc, cache && round > 0, cache && round == 0, [&](uint32_t k) {
             if ((k & pmask) == prefix)
                 atomicAdd(&hist[(k >> shift) & dmask], 1u);
-        };
-        if (vec) {
-            const float4 *r4 = reinterpret_cast<const float4 *>(row + lo);
-            const int64_t n4 = (hi - lo) / 4;
-#pragma unroll 4
-            for (int64_t i = tid; i < n4; i += kTkThreads) {
-                const float4 v = __ldg(r4 + i);
-                count(v.x);
-                count(v.y);
-                count(v.z);
-                count(v.w);
-            }
-            for (int64_t i = lo + 4 * n4 + tid; i < hi; i += kTkThreads)
-                count(__ldg(row + i));
-        } else {
-#pragma unroll 4
-            for (int64_t i = lo + tid; i < hi; i += kTkThreads)
-                count(__ldg(row + i));
-        }
-        if (CL > 1)
-            cluster_barrier();   // every segment's histogram is complete
-        else
-            __syncthreads();
+        });
+        sync_all();   // every segment's histogram is complete
         // this CTA's slice of the bins, summed over the cluster
         const int per = (nb + CL - 1) / CL;
         const int s_lo = min(nb, (int)rank * per);
         const int s_hi = min(nb, s_lo + per);
         uint32_t part = 0u;
         for (int b = s_lo + tid; b < s_hi; b += kTkThreads) {
+            uint32_t v[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)   // every remote load in flight before the sum
+                v[r] = (r < CL && r != (int)rank) ? ld_remote(remote_addr(&hist[b], (uint32_t)r)) : 0u;
             uint32_t s = hist[b];
-            for (int r = 0; r < CL; ++r)
-                if (r != (int)rank)
-                    s += ld_remote(remote_addr(&hist[b], (uint32_t)r));
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                s += v[r];
             slice[b - s_lo] = s;
             part += s;
         }
@@ -211,10 +293,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParam
         block_scan(part, wsum, tot);
         if (tid < CL)
             put(&sums[rank], tid, tot);
-        if (CL > 1)
-            cluster_barrier();   // slice totals everywhere
-        else
-            __syncthreads();
+        sync_all();   // slice totals everywhere
         // the slice holding the rem-th largest key (higher ranks hold higher bins)
         uint32_t above = 0u;
         int owner = 0;
@@ -250,70 +329,99 @@ __global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParam
                 }
             }
         }
-        if (CL > 1)
-            cluster_barrier();   // the digit is known everywhere; remote reads of hist are over
-        else
-            __syncthreads();
-        prefix |= bcast[0] << shift;
+        sync_all();   // the digit is known everywhere; remote reads of hist are over
+        const uint32_t digit = bcast[0];
+        prefix |= digit << shift;
         pmask |= dmask << shift;
         rem = bcast[1];
+        uint32_t mine = 0u;   // this segment's keys in the bins above the digit
+        for (int b = (int)digit + 1 + tid; b < nb; b += kTkThreads)
+            mine += hist[b];
+        uint32_t atot;
+        block_scan(mine, wsum, atot);
+        gt_local += atot;
+        if (round == 2)
+            eq_local = hist[digit];
     }
     const uint32_t vstar = prefix;   // the K-th largest key; rem keys equal to it are taken
 
-    // ---- counts of this segment, then the output offsets of every segment
-    uint32_t g = 0u, e = 0u;
-    for (int64_t i = lo + tid; i < hi; i += kTkThreads) {
-        const uint32_t k = order_key(__ldg(row + i));
-        g += k > vstar;
-        e += k == vstar;
-    }
-    uint32_t gtot, etot;
-    block_scan(g, wsum, gtot);
-    block_scan(e, wsum, etot);
+    // ---- output offsets of every segment
     if (tid < CL) {
-        put(&cnt[rank][0], tid, gtot);
-        put(&cnt[rank][1], tid, etot);
+        put(&cnt[rank][0], tid, gt_local);
+        put(&cnt[rank][1], tid, eq_local);
     }
-    if (CL > 1)
-        cluster_barrier();
-    else
-        __syncthreads();
+    sync_all();
     uint32_t G = 0u, E = 0u;   // keys > v* and == v* before this segment
     for (int r = 0; r < (int)rank; ++r) {
         G += cnt[r][0];
         E += cnt[r][1];
     }
+
     // ---- position-ordered compaction: the output index of a selected position is
-    // (keys > v* before it) + min(keys == v* before it, rem)
-#pragma unroll 1
-    for (int64_t base = lo; base < hi; base += kTkTile) {
-        const int64_t i0 = base + (int64_t)tid * kTkItems;
-        uint32_t keys[kTkItems];
-        uint32_t pk = 0u;   // (> v*) << 16 | (== v*) among this thread's positions
+    // (keys > v* before it) + min(keys == v* before it, rem).  Warp w owns a contiguous chunk of
+    // the segment; a first walk counts each chunk, a second writes with warp scans only.
+    const int64_t len = hi - lo;
+    const int64_t cw = (len + kTkWarps - 1) / kTkWarps;
+    const int64_t c_lo = min(len, (int64_t)warp * cw);
+    const int64_t c_hi = min(len, c_lo + cw);
+    auto key_at = [&](int64_t i) -> uint32_t { return cache ? kc[i] : order_key(__ldg(row + lo + i)); };
+    uint32_t ng = 0u, ne = 0u;   // keys > v* and == v* among this lane's positions of the chunk
+    for (int64_t i = c_lo + lane; i < c_hi; i += 32) {
+        const uint32_t k = key_at(i);
+        ng += k > vstar;
+        ne += k == vstar;
+    }
+    uint32_t wg = 0u, we = 0u;
 #pragma unroll
-        for (int j = 0; j < kTkItems; ++j) {
-            keys[j] = i0 + j < hi ? order_key(__ldg(row + i0 + j)) : 0u;
-            const bool in = i0 + j < hi;
-            pk += (in && keys[j] > vstar) ? 0x10000u : ((in && keys[j] == vstar) ? 1u : 0u);
+    for (int o = 16; o > 0; o >>= 1) {
+        ng += __shfl_xor_sync(0xffffffffu, ng, o);
+        ne += __shfl_xor_sync(0xffffffffu, ne, o);
+    }
+    if (lane == 0) {
+        wcnt[warp][0] = ng;
+        wcnt[warp][1] = ne;
+    }
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) {
+        wg += wcnt[w][0];
+        we += wcnt[w][1];
+    }
+    uint32_t gb = G + wg, eb = E + we;   // keys > v* and == v* before this lane's next positions
+    for (int64_t s0 = c_lo; s0 < c_hi; s0 += kTkStep) {
+        const int64_t i0 = s0 + (int64_t)lane * 8;
+        uint32_t keys[8];
+        uint32_t q = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const bool in = i0 + j < c_hi;
+            keys[j] = in ? key_at(i0 + j) : 0u;
+            q += (in && keys[j] > vstar) ? 0x10000u : ((in && keys[j] == vstar) ? 1u : 0u);
         }
-        uint32_t ptot;
-        const uint32_t excl = block_scan(pk, wsum, ptot) - pk;
-        uint32_t gb = G + (excl >> 16), eb = E + (excl & 0xFFFFu);
+        uint32_t incl = q;
 #pragma unroll
-        for (int j = 0; j < kTkItems; ++j) {
-            if (i0 + j >= hi)
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        const uint32_t step_tot = __shfl_sync(0xffffffffu, incl, 31);
+        const uint32_t excl = incl - q;
+        uint32_t g = gb + (excl >> 16), e = eb + (excl & 0xFFFFu);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (i0 + j >= c_hi)
                 break;
             if (keys[j] > vstar) {
-                orow[gb + min(eb, rem)] = (int32_t)(i0 + j);
-                ++gb;
+                orow[g + min(e, rem)] = (int32_t)(lo + i0 + j);
+                ++g;
             } else if (keys[j] == vstar) {
-                if (eb < rem)
-                    orow[gb + eb] = (int32_t)(i0 + j);
-                ++eb;
+                if (e < rem)
+                    orow[g + e] = (int32_t)(lo + i0 + j);
+                ++e;
             }
         }
-        G += ptot >> 16;
-        E += ptot & 0xFFFFu;
+        gb += step_tot >> 16;
+        eb += step_tot & 0xFFFFu;
     }
 }
 
@@ -333,13 +441,22 @@ cudaError_t launch_topk_select(const float *scores, int64_t score_stride, int wi
 {
     if (num_tokens <= 0)
         return cudaSuccess;
-    if (cluster < 1 || cluster > 8 || top_k < 1)
+    if (cluster < 1 || cluster > 8 || top_k < 1 || width < 0)
         return cudaErrorInvalidValue;
-    TopkParams p{scores, score_stride, width, num_cand, top_k, out, out_stride, lens, cluster};
+    // every segment's keys in shared memory when the longest segment fits the cache
+    const long long seg_max = (((long long)width + cluster - 1) / cluster + 3) / 4 * 4;
+    const int cache = seg_max <= kTkCacheKeys ? 1 : 0;
+    const int smem = cache ? (int)(seg_max * 4) : 0;
+    if (smem > 0) {
+        cudaError_t e = set_smem_once(reinterpret_cast<const void *>(topk_select_kernel), kTkCacheKeys * 4, kAttrTopk);
+        if (e != cudaSuccess)
+            return e;
+    }
+    TopkParams p{scores, score_stride, width, num_cand, top_k, out, out_stride, lens, cluster, cache};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long long)num_tokens * cluster));
     cfg.blockDim = dim3(kTkThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
