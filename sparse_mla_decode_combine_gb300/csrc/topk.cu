@@ -9,14 +9,16 @@
 // One thread-block cluster of CL CTAs per token row (CL = 1 when the rows alone fill the
 // GPU), each CTA a contiguous segment of the row.  Scores become order-preserving 32-bit
 // keys; three histogram rounds (11, 11 and 10 bits from the top) find the K-th largest key
-// v* and how many keys equal to v* the selection takes.  Each round every CTA builds its
-// segment's histogram in shared memory, then reduces one slice of the bins across the
-// cluster through distributed shared memory; the owner of the slice holding the K-th key
-// broadcasts the digit.  The first round reads the scores from HBM with 16-byte loads issued
-// four deep and keeps the segment's keys in shared memory (up to 40960 keys a CTA), so the
-// later rounds and the compaction read no global memory.  The compaction walks the segment
-// in position order, one contiguous chunk per warp with warp scans only, and writes every
-// position with key > v* and the first ones with key == v*.
+// v* and how many keys equal to v* the selection takes.  For each round every CTA builds its
+// segment's histogram in shared memory and reduces one slice of the bins across the cluster
+// through distributed shared memory; the owner of the slice holding the K-th key broadcasts
+// the digit.  Round 0 reads the scores from HBM with 16-byte loads issued four deep and keeps
+// the segment's keys in shared memory (up to 40960 keys a CTA).  One pass over the cached
+// keys then lists the keys of round 0's bin with their positions (up to 256 a warp chunk) and
+// counts the keys above it; rounds 1 and 2 and the per-chunk counts work on that list alone
+// (a segment with more candidates, i.e. many equal keys, rescans its keys instead).  The
+// compaction walks the segment in position order, one contiguous chunk per warp with warp
+// scans only, and writes every position with key > v* and the first ones with key == v*.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,11 +27,14 @@
 namespace dsv4 {
 namespace {
 
-constexpr int kTkThreads = 512;
-constexpr int kTkWarps = kTkThreads / 32;
+// CTA size: 1024 threads when a row has a CTA to itself, 512 in clusters (two CTAs fit an SM,
+// so a cluster's CTAs find room inside one GPC)
+constexpr int kTkThreadsRow = 1024;
+constexpr int kTkThreadsCluster = 512;
 constexpr int kTkBins = 2048;          // 11-bit digits
 constexpr int kTkCacheKeys = 40960;    // keys of a segment kept in shared memory (160 KB)
 constexpr int kTkStep = 32 * 8;        // compaction: a warp takes 8 consecutive positions per lane
+constexpr int kTkCandMax = 4096;       // candidates (keys in round 0's bin) kept in shared memory
 
 struct TopkParams {
     const float *scores;
@@ -41,7 +46,7 @@ struct TopkParams {
     int64_t out_stride;
     int32_t *lens;
     int32_t cluster;
-    int32_t cache;   // 1: every segment's keys fit the shared-memory cache
+    int32_t cache;   // keys of shared-memory cache per CTA (0: no cache; every segment fits otherwise)
 };
 
 // Order-preserving key: larger score -> larger key; -0 and +0 share a key; NaN -> 0, below
@@ -89,9 +94,11 @@ __device__ __forceinline__ void st_remote(uint32_t addr, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// Inclusive prefix sum over the CTA's threads; `total` gets the sum of all.
+// Inclusive prefix sum over the CTA's NT threads; `total` gets the sum of all.
+template <int NT>
 __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *wsum, uint32_t &total)
 {
+    constexpr int kTkWarps = NT / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -123,7 +130,7 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t *wsum, uint3
 // Visits every key of the segment row[lo, hi): from the shared-memory cache (kc[i - lo]) when
 // `cached`, else from global memory, storing it into the cache when `fill`.  Loads are issued
 // four deep before any key is used.  f(key) must not synchronise.
-template <class F>
+template <int NT, class F>
 __device__ __forceinline__ void visit_keys(const float *row, int64_t lo, int64_t hi, bool vec, uint32_t *kc,
                                            bool cached, bool fill, F f)
 {
@@ -132,38 +139,38 @@ __device__ __forceinline__ void visit_keys(const float *row, int64_t lo, int64_t
     const int64_t n4 = len / 4;
     if (cached) {
         const uint4 *k4 = reinterpret_cast<const uint4 *>(kc);
-        for (int64_t b = 0; b < n4; b += 4 * kTkThreads) {
+        for (int64_t b = 0; b < n4; b += 4 * NT) {
             uint4 v[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int64_t i = b + j * kTkThreads + tid;
+                const int64_t i = b + j * NT + tid;
                 v[j] = i < n4 ? k4[i] : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                if (b + j * kTkThreads + tid < n4) {
+                if (b + j * NT + tid < n4) {
                     f(v[j].x);
                     f(v[j].y);
                     f(v[j].z);
                     f(v[j].w);
                 }
         }
-        for (int64_t i = 4 * n4 + tid; i < len; i += kTkThreads)
+        for (int64_t i = 4 * n4 + tid; i < len; i += NT)
             f(kc[i]);
         return;
     }
     if (vec) {
         const float4 *r4 = reinterpret_cast<const float4 *>(row + lo);
-        for (int64_t b = 0; b < n4; b += 4 * kTkThreads) {
+        for (int64_t b = 0; b < n4; b += 4 * NT) {
             float4 v[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int64_t i = b + j * kTkThreads + tid;
+                const int64_t i = b + j * NT + tid;
                 v[j] = i < n4 ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int64_t i = b + j * kTkThreads + tid;
+                const int64_t i = b + j * NT + tid;
                 if (i < n4) {
                     const uint4 k = make_uint4(order_key(v[j].x), order_key(v[j].y), order_key(v[j].z),
                                                order_key(v[j].w));
@@ -177,16 +184,16 @@ __device__ __forceinline__ void visit_keys(const float *row, int64_t lo, int64_t
             }
         }
     } else {
-        for (int64_t b = 0; b < 4 * n4; b += 4 * kTkThreads) {
+        for (int64_t b = 0; b < 4 * n4; b += 4 * NT) {
             float v[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int64_t i = b + j * kTkThreads + tid;
+                const int64_t i = b + j * NT + tid;
                 v[j] = i < 4 * n4 ? __ldg(row + lo + i) : 0.f;
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int64_t i = b + j * kTkThreads + tid;
+                const int64_t i = b + j * NT + tid;
                 if (i < 4 * n4) {
                     const uint32_t k = order_key(v[j]);
                     if (fill)
@@ -196,7 +203,7 @@ __device__ __forceinline__ void visit_keys(const float *row, int64_t lo, int64_t
             }
         }
     }
-    for (int64_t i = 4 * n4 + tid; i < len; i += kTkThreads) {
+    for (int64_t i = 4 * n4 + tid; i < len; i += NT) {
         const uint32_t k = order_key(__ldg(row + lo + i));
         if (fill)
             kc[i] = k;
@@ -204,17 +211,25 @@ __device__ __forceinline__ void visit_keys(const float *row, int64_t lo, int64_t
     }
 }
 
-__global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParams p)
+template <int NT>
+__global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
 {
+    constexpr int kTkThreads = NT;
+    constexpr int kTkWarps = NT / 32;
+    constexpr int kTkCandWarp = kTkCandMax / kTkWarps;   // a sub-list per warp chunk
     __shared__ uint32_t hist[kTkBins];     // this CTA's histogram of the round
     __shared__ uint32_t slice[kTkBins];    // this CTA's slice of the cluster-wide histogram
     __shared__ uint32_t sums[8];           // slice totals of every CTA of the cluster
     __shared__ uint32_t bcast[2];          // the round's digit and remaining count
     __shared__ uint32_t cnt[8][2];         // (> v*, == v*) counts per CTA
     __shared__ uint32_t wsum[kTkWarps];
-    __shared__ uint32_t wcnt[kTkWarps][2];   // compaction: (> v*, == v*) counts per warp chunk
-    extern __shared__ uint4 kcache4[];     // the segment's keys (when p.cache)
-    uint32_t *kc = reinterpret_cast<uint32_t *>(kcache4);
+    __shared__ uint32_t wsure[kTkWarps];     // keys above round 0's bin per warp chunk
+    __shared__ uint32_t wcnt[kTkWarps][2];   // (> v*, == v*) counts per warp chunk
+    __shared__ uint32_t wncand[kTkWarps];    // candidates per warp chunk
+    extern __shared__ uint4 dyn4[];        // [p.cache keys][kTkCandMax candidate keys][kTkCandMax positions]
+    uint32_t *kc = reinterpret_cast<uint32_t *>(dyn4);
+    uint32_t *ckey = kc + p.cache;
+    uint32_t *cpos = ckey + kTkCandMax;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -253,99 +268,207 @@ __global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParam
     const int64_t lo = min(n, (int64_t)rank * seg);
     const int64_t hi = min(n, lo + seg);
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-    const bool cache = p.cache != 0;
+    const bool cache = p.cache > 0;
+    const int len = (int)(hi - lo);
+    // warp w owns the chunk [c_lo, c_hi) of the segment (a multiple of 8 positions long)
+    const int cw = ((len + kTkWarps - 1) / kTkWarps + 7) / 8 * 8;
+    const int c_lo = min(len, warp * cw);
+    const int c_hi = min(len, c_lo + cw);
+    auto key_at = [&](int i) -> uint32_t { return cache ? kc[i] : order_key(__ldg(row + lo + i)); };
 
-    // ---- three digit rounds find the K-th largest key v* and how many keys equal to it are
-    // taken (rem); this CTA's keys above v* (gt) and equal to it (eq) come from its histograms
-    uint32_t prefix = 0u, pmask = 0u, rem = (uint32_t)m;
-    uint32_t gt_local = 0u, eq_local = 0u;
-#pragma unroll 1
-    for (int round = 0; round < 3; ++round) {
-        const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
-        const int nb = round == 2 ? 1024 : 2048;
-        const uint32_t dmask = (uint32_t)nb - 1u;
-        for (int i = tid; i < nb; i += kTkThreads)
-            hist[i] = 0u;
-        __syncthreads();
-        visit_keys(row, lo, hi, vec, kc, cache && round > 0, cache && round == 0, [&](uint32_t k) {
-            if ((k & pmask) == prefix)
-                atomicAdd(&hist[(k >> shift) & dmask], 1u);
-        });
+    // The digit of a round: the cluster-wide histogram of the round (this CTA's part in
+    // `hist`) decides which bin holds the rem-th largest key; rem becomes its rank in the bin.
+    uint32_t rem = (uint32_t)m;
+    auto find_digit = [&](int nb) -> uint32_t {
         sync_all();   // every segment's histogram is complete
-        // this CTA's slice of the bins, summed over the cluster
-        const int per = (nb + CL - 1) / CL;
-        const int s_lo = min(nb, (int)rank * per);
-        const int s_hi = min(nb, s_lo + per);
-        uint32_t part = 0u;
-        for (int b = s_lo + tid; b < s_hi; b += kTkThreads) {
-            uint32_t v[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r)   // every remote load in flight before the sum
-                v[r] = (r < CL && r != (int)rank) ? ld_remote(remote_addr(&hist[b], (uint32_t)r)) : 0u;
-            uint32_t s = hist[b];
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-                s += v[r];
-            slice[b - s_lo] = s;
-            part += s;
-        }
-        uint32_t tot;
-        block_scan(part, wsum, tot);
-        if (tid < CL)
-            put(&sums[rank], tid, tot);
-        sync_all();   // slice totals everywhere
-        // the slice holding the rem-th largest key (higher ranks hold higher bins)
+        const uint32_t *bins = hist;
+        int s_lo = 0, s_hi = nb, owner = 0;
         uint32_t above = 0u;
-        int owner = 0;
-        for (int r = CL - 1; r >= 0; --r) {
-            if (above + sums[r] >= rem) {
-                owner = r;
-                break;
+        if (CL > 1) {   // this CTA's slice of the bins, summed over the cluster
+            const int per = (nb + CL - 1) / CL;
+            s_lo = min(nb, (int)rank * per);
+            s_hi = min(nb, s_lo + per);
+            uint32_t part = 0u;
+            for (int b = s_lo + tid; b < s_hi; b += kTkThreads) {
+                uint32_t v[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r)   // every remote load in flight before the sum
+                    v[r] = (r < CL && r != (int)rank) ? ld_remote(remote_addr(&hist[b], (uint32_t)r)) : 0u;
+                uint32_t sm = hist[b];
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    sm += v[r];
+                slice[b - s_lo] = sm;
+                part += sm;
             }
-            above += sums[r];
+            uint32_t tot;
+            block_scan<NT>(part, wsum, tot);
+            if (tid < CL)
+                put(&sums[rank], tid, tot);
+            cluster_barrier();   // slice totals everywhere
+            for (int r = CL - 1; r >= 0; --r) {   // higher ranks hold higher bins
+                if (above + sums[r] >= rem) {
+                    owner = r;
+                    break;
+                }
+                above += sums[r];
+            }
+            bins = slice;
         }
         if ((int)rank == owner) {
             // thread i takes the i-th group of c bins counted from the top of the slice
-            const int len = s_hi - s_lo;
-            const int c = (len + kTkThreads - 1) / kTkThreads;
-            const int g_hi = len - tid * c;
+            const int nbs = s_hi - s_lo;
+            const int c = (nbs + kTkThreads - 1) / kTkThreads;
+            const int g_hi = nbs - tid * c;
             const int g_lo = max(0, g_hi - c);
             uint32_t gs = 0u;
             for (int b = g_lo; b < g_hi; ++b)
-                gs += slice[b];
+                gs += bins[b];
             uint32_t gtot;
-            const uint32_t incl = block_scan(gs, wsum, gtot);
+            const uint32_t incl = block_scan<NT>(gs, wsum, gtot);
             uint32_t a = above + incl - gs;   // keys in bins above this group
             if (g_lo < g_hi && a < rem && rem <= a + gs) {
                 for (int b = g_hi - 1; b >= g_lo; --b) {
-                    if (a + slice[b] >= rem) {
+                    if (a + bins[b] >= rem) {
                         for (int r = 0; r < CL; ++r) {
                             put(&bcast[0], r, (uint32_t)(s_lo + b));
                             put(&bcast[1], r, rem - a);
                         }
                         break;
                     }
-                    a += slice[b];
+                    a += bins[b];
                 }
             }
         }
         sync_all();   // the digit is known everywhere; remote reads of hist are over
-        const uint32_t digit = bcast[0];
-        prefix |= digit << shift;
-        pmask |= dmask << shift;
         rem = bcast[1];
-        uint32_t mine = 0u;   // this segment's keys in the bins above the digit
-        for (int b = (int)digit + 1 + tid; b < nb; b += kTkThreads)
-            mine += hist[b];
-        uint32_t atot;
-        block_scan(mine, wsum, atot);
-        gt_local += atot;
-        if (round == 2)
-            eq_local = hist[digit];
+        return bcast[0];
+    };
+
+    // ---- round 0 (top 11 bits) over every key; the keys go to the shared-memory cache
+    for (int i = tid; i < kTkBins; i += kTkThreads)
+        hist[i] = 0u;
+    __syncthreads();
+    visit_keys<NT>(row, lo, hi, vec, kc, false, cache, [&](uint32_t k) { atomicAdd(&hist[k >> 21], 1u); });
+    const uint32_t d0 = find_digit(kTkBins);
+    uint32_t prefix = d0 << 21, pmask = 0xFFE00000u;
+
+    // ---- the keys in round 0's bin become candidates (key, position), each warp listing those
+    // of its chunk; keys above the bin are selected whatever the later rounds find
+    uint32_t sure = 0u, nw = 0u;   // per lane: keys above the bin; per warp: candidates so far
+    uint32_t *wkey = ckey + warp * kTkCandWarp;
+    uint32_t *wpos = cpos + warp * kTkCandWarp;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int i0 = c_lo; i0 < c_hi; i0 += 128) {   // four consecutive keys a lane
+        const int i = i0 + 4 * lane;
+        uint32_t k[4];
+        if (cache && i + 4 <= c_hi) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(kc + i);
+            k[0] = v.x;
+            k[1] = v.y;
+            k[2] = v.z;
+            k[3] = v.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                k[j] = i + j < c_hi ? key_at(i + j) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool in = i + j < c_hi;
+            sure += (in && (k[j] >> 21) > d0) ? 1u : 0u;
+            const bool cand = in && (k[j] >> 21) == d0;
+            const uint32_t bal = __ballot_sync(0xffffffffu, cand);
+            const uint32_t slot = nw + (uint32_t)__popc(bal & lt);
+            if (cand && slot < (uint32_t)kTkCandWarp) {
+                wkey[slot] = k[j];
+                wpos[slot] = (uint32_t)(i + j);
+            }
+            nw += (uint32_t)__popc(bal);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sure += __shfl_xor_sync(0xffffffffu, sure, o);
+    if (lane == 0) {
+        wsure[warp] = sure;
+        wncand[warp] = nw;
+    }
+    __syncthreads();
+    bool listed = true;   // else (many equal keys in one chunk) the rounds rescan the segment
+    for (int w = 0; w < kTkWarps; ++w)
+        listed = listed && wncand[w] <= (uint32_t)kTkCandWarp;
+
+    // ---- rounds 1 (next 11 bits) and 2 (last 10 bits)
+#pragma unroll 1
+    for (int round = 1; round < 3; ++round) {
+        const int shift = round == 1 ? 10 : 0;
+        const int nb = round == 1 ? 2048 : 1024;
+        const uint32_t dmask = (uint32_t)nb - 1u;
+        for (int i = tid; i < nb; i += kTkThreads)
+            hist[i] = 0u;
+        __syncthreads();
+        auto count = [&](uint32_t k) {
+            if ((k & pmask) == prefix)
+                atomicAdd(&hist[(k >> shift) & dmask], 1u);
+        };
+        if (listed) {
+            for (int c = tid; c < kTkCandMax; c += kTkThreads)
+                if ((uint32_t)(c % kTkCandWarp) < wncand[c / kTkCandWarp])
+                    count(ckey[c]);
+        } else {
+            visit_keys<NT>(row, lo, hi, vec, kc, cache, false, count);
+        }
+        const uint32_t d = find_digit(nb);
+        prefix |= d << shift;
+        pmask |= dmask << shift;
     }
     const uint32_t vstar = prefix;   // the K-th largest key; rem keys equal to it are taken
 
-    // ---- output offsets of every segment
+    // ---- (> v*, == v*) per warp chunk, then per segment and the segments' offsets
+    if (tid < kTkWarps) {
+        wcnt[tid][0] = listed ? wsure[tid] : 0u;
+        wcnt[tid][1] = 0u;
+    }
+    __syncthreads();
+    if (listed) {
+        for (int c = tid; c < kTkCandMax; c += kTkThreads) {
+            const int w = c / kTkCandWarp;
+            if ((uint32_t)(c % kTkCandWarp) < wncand[w]) {
+                const uint32_t k = ckey[c];
+                if (k > vstar)
+                    atomicAdd(&wcnt[w][0], 1u);
+                else if (k == vstar)
+                    atomicAdd(&wcnt[w][1], 1u);
+            }
+        }
+    } else {
+        uint32_t ng = 0u, ne = 0u;
+        for (int i = c_lo + lane; i < c_hi; i += 32) {
+            const uint32_t k = key_at(i);
+            ng += k > vstar;
+            ne += k == vstar;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ng += __shfl_xor_sync(0xffffffffu, ng, o);
+            ne += __shfl_xor_sync(0xffffffffu, ne, o);
+        }
+        if (lane == 0) {
+            wcnt[warp][0] = ng;
+            wcnt[warp][1] = ne;
+        }
+    }
+    __syncthreads();
+    uint32_t gt_local = 0u, eq_local = 0u, wg = 0u, we = 0u;
+    for (int w = 0; w < kTkWarps; ++w) {
+        if (w == warp) {
+            wg = gt_local;
+            we = eq_local;
+        }
+        gt_local += wcnt[w][0];
+        eq_local += wcnt[w][1];
+    }
     if (tid < CL) {
         put(&cnt[rank][0], tid, gt_local);
         put(&cnt[rank][1], tid, eq_local);
@@ -357,46 +480,27 @@ __global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParam
         E += cnt[r][1];
     }
 
-    // ---- position-ordered compaction: the output index of a selected position is
-    // (keys > v* before it) + min(keys == v* before it, rem).  Warp w owns a contiguous chunk of
-    // the segment; a first walk counts each chunk, a second writes with warp scans only.
-    const int64_t len = hi - lo;
-    const int64_t cw = (len + kTkWarps - 1) / kTkWarps;
-    const int64_t c_lo = min(len, (int64_t)warp * cw);
-    const int64_t c_hi = min(len, c_lo + cw);
-    auto key_at = [&](int64_t i) -> uint32_t { return cache ? kc[i] : order_key(__ldg(row + lo + i)); };
-    uint32_t ng = 0u, ne = 0u;   // keys > v* and == v* among this lane's positions of the chunk
-    for (int64_t i = c_lo + lane; i < c_hi; i += 32) {
-        const uint32_t k = key_at(i);
-        ng += k > vstar;
-        ne += k == vstar;
-    }
-    uint32_t wg = 0u, we = 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        ng += __shfl_xor_sync(0xffffffffu, ng, o);
-        ne += __shfl_xor_sync(0xffffffffu, ne, o);
-    }
-    if (lane == 0) {
-        wcnt[warp][0] = ng;
-        wcnt[warp][1] = ne;
-    }
-    __syncthreads();
-    for (int w = 0; w < warp; ++w) {
-        wg += wcnt[w][0];
-        we += wcnt[w][1];
-    }
+    // ---- position-ordered compaction over this warp's chunk: the output index of a selected
+    // position is (keys > v* before it) + min(keys == v* before it, rem)
     uint32_t gb = G + wg, eb = E + we;   // keys > v* and == v* before this lane's next positions
-    for (int64_t s0 = c_lo; s0 < c_hi; s0 += kTkStep) {
-        const int64_t i0 = s0 + (int64_t)lane * 8;
+    for (int s0 = c_lo; s0 < c_hi; s0 += kTkStep) {
+        const int i0 = s0 + lane * 8;
         uint32_t keys[8];
+        if (cache && i0 + 8 <= c_hi) {
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(kc + i0);
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(kc + i0 + 4);
+            keys[0] = a0.x; keys[1] = a0.y; keys[2] = a0.z; keys[3] = a0.w;
+            keys[4] = a1.x; keys[5] = a1.y; keys[6] = a1.z; keys[7] = a1.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                keys[j] = i0 + j < c_hi ? key_at(i0 + j) : 0u;
+        }
         uint32_t q = 0u;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const bool in = i0 + j < c_hi;
-            keys[j] = in ? key_at(i0 + j) : 0u;
-            q += (in && keys[j] > vstar) ? 0x10000u : ((in && keys[j] == vstar) ? 1u : 0u);
-        }
+        for (int j = 0; j < 8; ++j)
+            q += (i0 + j < c_hi && keys[j] > vstar) ? 0x10000u
+                                                   : ((i0 + j < c_hi && keys[j] == vstar) ? 1u : 0u);
         uint32_t incl = q;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -405,19 +509,18 @@ __global__ void __launch_bounds__(kTkThreads) topk_select_kernel(const TopkParam
                 incl += y;
         }
         const uint32_t step_tot = __shfl_sync(0xffffffffu, incl, 31);
-        const uint32_t excl = incl - q;
-        uint32_t g = gb + (excl >> 16), e = eb + (excl & 0xFFFFu);
+        if (q != 0u) {
+            const uint32_t excl = incl - q;
+            uint32_t g = gb + (excl >> 16), e = eb + (excl & 0xFFFFu);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (i0 + j >= c_hi)
-                break;
-            if (keys[j] > vstar) {
-                orow[g + min(e, rem)] = (int32_t)(lo + i0 + j);
-                ++g;
-            } else if (keys[j] == vstar) {
-                if (e < rem)
-                    orow[g + e] = (int32_t)(lo + i0 + j);
-                ++e;
+            for (int j = 0; j < 8; ++j) {   // one predicated store a key: index g + min(e, rem) either way
+                const bool in = i0 + j < c_hi;
+                const bool gt = in && keys[j] > vstar;
+                const bool eq = in && keys[j] == vstar;
+                if (gt || (eq && e < rem))
+                    orow[g + min(e, rem)] = (int32_t)(lo + i0 + j);
+                g += gt ? 1u : 0u;
+                e += eq ? 1u : 0u;
             }
         }
         gb += step_tot >> 16;
@@ -445,17 +548,17 @@ cudaError_t launch_topk_select(const float *scores, int64_t score_stride, int wi
         return cudaErrorInvalidValue;
     // every segment's keys in shared memory when the longest segment fits the cache
     const long long seg_max = (((long long)width + cluster - 1) / cluster + 3) / 4 * 4;
-    const int cache = seg_max <= kTkCacheKeys ? 1 : 0;
-    const int smem = cache ? (int)(seg_max * 4) : 0;
-    if (smem > 0) {
-        cudaError_t e = set_smem_once(reinterpret_cast<const void *>(topk_select_kernel), kTkCacheKeys * 4, kAttrTopk);
-        if (e != cudaSuccess)
-            return e;
-    }
+    const int cache = seg_max <= kTkCacheKeys ? (int)seg_max : 0;
+    const int smem = 4 * cache + 8 * kTkCandMax;
+    const void *kernel = cluster > 1 ? reinterpret_cast<const void *>(topk_select_kernel<kTkThreadsCluster>)
+                                     : reinterpret_cast<const void *>(topk_select_kernel<kTkThreadsRow>);
+    cudaError_t e = set_smem_once(kernel, 4 * kTkCacheKeys + 8 * kTkCandMax, cluster > 1 ? kAttrTopkCluster : kAttrTopk);
+    if (e != cudaSuccess)
+        return e;
     TopkParams p{scores, score_stride, width, num_cand, top_k, out, out_stride, lens, cluster, cache};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long long)num_tokens * cluster));
-    cfg.blockDim = dim3(kTkThreads);
+    cfg.blockDim = dim3(cluster > 1 ? kTkThreadsCluster : kTkThreadsRow);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -466,7 +569,7 @@ cudaError_t launch_topk_select(const float *scores, int64_t score_stride, int wi
     cfg.attrs = attr;
     cfg.numAttrs = cluster > 1 ? 1 : 0;
     void *args[] = {&p};
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(topk_select_kernel), args);
+    return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 
 }  // namespace dsv4
