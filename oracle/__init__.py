@@ -10,6 +10,7 @@ section each follows):
   * ``combine`` - top-k + sliding-window index combine with dedup and compaction,
   * ``combine_compressed`` - the compressed-region variant of the combine,
   * ``topk_select`` - top-k selection from indexer scores (what produces the top-k rows),
+  * ``qnorm_rope`` / ``kv_insert`` - the fused Q RMSNorm + GPT-J RoPE and FP8 KV-cache insert,
   * ``attend`` - sink-softmax MQA attention of one head over explicit keys,
   * ``merge`` - log-sum-exp merge of partial results over disjoint key sets,
   * ``sparse_mla_decode`` - the whole decode for all (or a subset of) tokens.
@@ -75,6 +76,12 @@ class Oracle:
         lib.oracle_combine.argtypes = [P, i64, i32, P, P, i32, i32, P, i64, i32, P]
         lib.oracle_combine_compressed.restype = ctypes.c_int
         lib.oracle_combine_compressed.argtypes = [P, i64, i32, P, P, P, i32, i32, i32, i32, i32, i32, P, i64, i32, P]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [f64]
+        lib.oracle_qnorm_rope.restype = i64
+        lib.oracle_qnorm_rope.argtypes = [P, i64, i32, i32, P, f64, P, P, i32, P, i64]
+        lib.oracle_kv_insert.restype = i64
+        lib.oracle_kv_insert.argtypes = [P, i64, i32, P, P, P, i32, P, i64]
         lib.oracle_topk_select.restype = ctypes.c_int
         lib.oracle_topk_select.argtypes = [P, i64, i32, P, i32, i32, P, i64, P]
         lib.oracle_attend.restype = None
@@ -131,6 +138,31 @@ class Oracle:
         if rc != 0:
             raise ValueError("arguments outside the compressed combine's rules")
         return out, lens
+
+    def e4m3_encode(self, y: float) -> int:
+        """E4M3FN code of a finite |y| <= 448, round to nearest even."""
+        return int(self.lib.oracle_e4m3_encode(float(y)))
+
+    def qnorm_rope(self, q_bits, positions, cos_sin, norm_w=None, eps: float = 1e-6):
+        """q_bits uint16 BF16 [T, H, 576] -> (normalised, rotated q bits uint16 [T, H, 576], bad count)."""
+        q = _c(q_bits, np.uint16)
+        T, H, _ = q.shape
+        cs = _c(cos_sin, np.float32)
+        w = None if norm_w is None else _c(norm_w, np.float32)
+        out = np.empty_like(q)
+        bad = self.lib.oracle_qnorm_rope(_ptr(q), H * 576, T, H, None if w is None else _ptr(w), float(eps),
+                                         _ptr(_c(positions, np.int64)), _ptr(cs), cs.shape[0], _ptr(out), H * 576)
+        return out, int(bad)
+
+    def kv_insert(self, kv_bits, slots, positions, cos_sin, cache):
+        """kv_bits uint16 BF16 [T, 576] into a copy of cache uint8 [S, 656] -> (cache, bad count)."""
+        kv = _c(kv_bits, np.uint16)
+        cs = _c(cos_sin, np.float32)
+        c = np.array(cache, dtype=np.uint8, copy=True, order="C")
+        bad = self.lib.oracle_kv_insert(_ptr(kv), 576, kv.shape[0], _ptr(_c(slots, np.int64)),
+                                        _ptr(_c(positions, np.int64)), _ptr(cs), cs.shape[0], _ptr(c),
+                                        c.reshape(-1, 656).shape[0])
+        return c, int(bad)
 
     def topk_select(self, scores, num_cand, top_k: int):
         """Top-k selection -> (topk_idx int32 [T, K] ascending then -1, topk_lens int32 [T])."""
@@ -227,6 +259,18 @@ def combine_compressed(topk_idx, query_start_loc, seq_lens, gather_lens, region_
                        compress_ratio, window, combined_width):
     return default().combine_compressed(topk_idx, query_start_loc, seq_lens, gather_lens, region_stride,
                                         compressed_len, top_k, compress_ratio, window, combined_width)
+
+
+def e4m3_encode(y):
+    return default().e4m3_encode(y)
+
+
+def qnorm_rope(q_bits, positions, cos_sin, norm_w=None, eps=1e-6):
+    return default().qnorm_rope(q_bits, positions, cos_sin, norm_w, eps)
+
+
+def kv_insert(kv_bits, slots, positions, cos_sin, cache):
+    return default().kv_insert(kv_bits, slots, positions, cos_sin, cache)
 
 
 def topk_select(scores, num_cand, top_k):

@@ -29,6 +29,9 @@
  *    definition: s_j = scale * q . k_j over 576 dims; with an optional sink
  *    logit sigma (in the same units as s), Z = sum_j e^{s_j} + e^{sigma},
  *    lse = ln Z, out = sum_j e^{s_j - lse} v_j.
+ *  - fused Q per-head RMSNorm + GPT-J RoPE + FP8/UE8M0 KV insert (the step before the path):
+ *    "feat: add DeepSeek-V4 XPU attention decode path" (vllm #42953), 实现拆解 4; readings at
+ *    oracle_qnorm_rope / oracle_kv_insert.
  *  - top-k selection from indexer scores (what produces topk_idx): "[Model] DeepSeek V4"
  *    (vllm #40860), 实现拆解 2; the selection rule is written out with its readings at
  *    oracle_topk_select.
@@ -218,6 +221,152 @@ int oracle_topk_select(const float *scores, int64_t score_stride, int32_t width,
         free(items);
     }
     return 0;
+}
+
+/* ---- fused Q per-head RMSNorm + GPT-J RoPE + FP8/UE8M0 KV insert ("feat: add DeepSeek-V4 XPU
+ * attention decode path" (vllm #42953), 实现拆解 4: xpu_qnorm_rope_kv_fp8_insert, called from
+ * forward_mqa as (q, kv, kv_cache, slot_mapping, positions, ...) before the decode).  The page
+ * names the steps; the readings taken here:
+ *  - each query head (576 dims) is divided by sqrt(mean of its squares + eps), then multiplied
+ *    by an optional weight w[576], with no rounding in between;
+ *  - GPT-J RoPE rotates the interleaved pairs (512 + 2i, 513 + 2i), i < 32, of the normalised
+ *    query and of the key by the angle whose cosine and sine are cos_sin[pos][i] and
+ *    cos_sin[pos][32 + i] (a caller-made fp32 table, as rotary caches are);
+ *  - the key's latent (512 dims) is quantised as the cache format stores it: per 128 values the
+ *    smallest integer e with 448 * 2^e >= amax (0 for amax 0, clamped to [-127, 127]), codes =
+ *    E4M3 round-to-nearest-even of x * 2^-e, scale byte e + 127; the rotated rope part is
+ *    rounded to BF16; the entry's 12 padding bytes are zero;
+ *  - the entry goes to slot slot_mapping[t]; a negative slot writes nothing (a padding token);
+ *    a slot past the cache or a position outside the table writes nothing and is counted;
+ *    such a token's query is normalised but not rotated.
+ * Every result is rounded once, from fp64. */
+static uint16_t bf16_from_double(double x)
+{
+    if (x == 0.0)
+        return signbit(x) ? 0x8000u : 0u;
+    int k;
+    frexp(x, &k);                          /* |x| in [2^(k-1), 2^k) */
+    int e = k - 1;
+    if (e < -126)
+        e = -126;                          /* BF16 subnormals share the quantum 2^-133 */
+    const double quantum = ldexp(1.0, e - 7);
+    const double r = rint(x / quantum) * quantum;   /* nearest, ties to even */
+    const float f = (float)r;              /* exact: at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* E4M3FN code of a finite |y| <= 448, round to nearest, ties to even. */
+uint8_t oracle_e4m3_encode(double y)
+{
+    const uint8_t s = signbit(y) ? 0x80u : 0u;
+    const double a = fabs(y);
+    if (a < ldexp(1.0, -6))                /* subnormal codes: value = q * 2^-9 (q = 8: 2^-6, code 8) */
+        return (uint8_t)(s | (uint8_t)rint(a * 512.0));
+    int k;
+    const double m = frexp(a, &k);         /* a = m * 2^k, m in [0.5, 1) */
+    int q = (int)rint((2.0 * m - 1.0) * 8.0);   /* a = (1 + q/8) * 2^(k-1) */
+    int ef = k - 1 + 7;
+    if (q == 8) {
+        q = 0;
+        ++ef;
+    }
+    return (uint8_t)(s | (uint8_t)(ef << 3) | (uint8_t)q);
+}
+
+/* Smallest integer e with 448 * 2^e >= amax (0 for amax 0), clamped to [-127, 127]. */
+static int ue8m0_exponent_of(double amax)
+{
+    if (amax <= 0.0)
+        return 0;
+    int e = -127;
+    while (e < 127 && 448.0 * ldexp(1.0, e) < amax)
+        ++e;
+    return e;
+}
+
+/* Rotates the pair (x, y) by the angle of (c, s). */
+static void rope_pair(double *x, double *y, double c, double s)
+{
+    const double a = *x, b = *y;
+    *x = a * c - b * s;
+    *y = a * s + b * c;
+}
+
+/* Queries: q, q_out BF16 bits [T, H, 576] (token strides in elements).  Returns the number of
+ * tokens whose position is outside [0, max_pos). */
+int64_t oracle_qnorm_rope(const uint16_t *q, int64_t q_stride, int32_t T, int32_t H, const float *norm_w, double eps,
+                          const int64_t *positions, const float *cos_sin, int32_t max_pos, uint16_t *q_out,
+                          int64_t q_out_stride)
+{
+    int64_t bad = 0;
+    double x[OR_DIM];
+    for (int32_t t = 0; t < T; ++t) {
+        const int64_t pos = positions[t];
+        const int rot = pos >= 0 && pos < max_pos;
+        bad += !rot;
+        for (int32_t h = 0; h < H; ++h) {
+            const uint16_t *in = q + t * q_stride + (int64_t)h * OR_DIM;
+            double ss = 0.0;
+            for (int d = 0; d < OR_DIM; ++d) {
+                x[d] = oracle_bf16_to_double(in[d]);
+                ss += x[d] * x[d];
+            }
+            const double r = 1.0 / sqrt(ss / OR_DIM + eps);
+            for (int d = 0; d < OR_DIM; ++d)
+                x[d] = x[d] * r * (norm_w ? (double)norm_w[d] : 1.0);
+            if (rot)
+                for (int i = 0; i < OR_ROPE / 2; ++i)
+                    rope_pair(&x[OR_LATENT + 2 * i], &x[OR_LATENT + 2 * i + 1], (double)cos_sin[pos * 64 + i],
+                              (double)cos_sin[pos * 64 + 32 + i]);
+            uint16_t *o = q_out + t * q_out_stride + (int64_t)h * OR_DIM;
+            for (int d = 0; d < OR_DIM; ++d)
+                o[d] = bf16_from_double(x[d]);
+        }
+    }
+    return bad;
+}
+
+/* Keys: kv BF16 bits [T, 576] (token stride in elements) into cache entries uint8 [num_slots, 656].
+ * Returns the number of tokens with a slot past the cache or a position outside the table. */
+int64_t oracle_kv_insert(const uint16_t *kv, int64_t kv_stride, int32_t T, const int64_t *slots,
+                         const int64_t *positions, const float *cos_sin, int32_t max_pos, uint8_t *cache,
+                         int64_t num_slots)
+{
+    int64_t bad = 0;
+    double x[OR_DIM];
+    for (int32_t t = 0; t < T; ++t) {
+        const int64_t slot = slots[t], pos = positions[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_slots || pos < 0 || pos >= max_pos) {
+            ++bad;
+            continue;
+        }
+        for (int d = 0; d < OR_DIM; ++d)
+            x[d] = oracle_bf16_to_double(kv[t * kv_stride + d]);
+        uint8_t *e = cache + slot * OR_ENTRY_BYTES;
+        memset(e, 0, OR_ENTRY_BYTES);
+        for (int b = 0; b < OR_LATENT / OR_SCALE_BLOCK; ++b) {
+            double amax = 0.0;
+            for (int d = b * OR_SCALE_BLOCK; d < (b + 1) * OR_SCALE_BLOCK; ++d)
+                amax = fabs(x[d]) > amax ? fabs(x[d]) : amax;
+            const int ex = ue8m0_exponent_of(amax);
+            for (int d = b * OR_SCALE_BLOCK; d < (b + 1) * OR_SCALE_BLOCK; ++d)
+                e[d] = oracle_e4m3_encode(ldexp(x[d], -ex));
+            e[OR_SCALE_OFF + b] = (uint8_t)(ex + 127);
+        }
+        for (int i = 0; i < OR_ROPE / 2; ++i)
+            rope_pair(&x[OR_LATENT + 2 * i], &x[OR_LATENT + 2 * i + 1], (double)cos_sin[pos * 64 + i],
+                      (double)cos_sin[pos * 64 + 32 + i]);
+        for (int i = 0; i < OR_ROPE; ++i) {
+            const uint16_t h = bf16_from_double(x[OR_LATENT + i]);
+            e[OR_ROPE_OFF + 2 * i] = (uint8_t)(h & 0xFF);
+            e[OR_ROPE_OFF + 2 * i + 1] = (uint8_t)(h >> 8);
+        }
+    }
+    return bad;
 }
 
 /* Combined index list of one token.  Returns its length L; row[0..L) holds

@@ -535,9 +535,145 @@ def check_topk_invariants(orc):
                 assert worst_in < best_out, (t, worst_in, best_out)
 
 
+# ----------------------------------------------------------------------------
+# fused Q RMSNorm + GPT-J RoPE + FP8/UE8M0 KV insert
+# ----------------------------------------------------------------------------
+def _bf16(x):
+    return synth.bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def _from_bf16(bits):
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _rope_table(angles):
+    """fp32 [P, 64]: cos then sin of angles [P, 32]."""
+    a = np.asarray(angles, dtype=np.float64)
+    return np.concatenate([np.cos(a), np.sin(a)], axis=1).astype(np.float32)
+
+
+def check_e4m3_encode(orc):
+    """The oracle's E4M3 encoder equals torch's float8_e4m3fn cast (round to nearest even) on every
+    code value, every midpoint between neighbouring codes and random values of every binade."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    pos = np.unique(vals[vals >= 0])
+    mids = (pos[1:] + pos[:-1]) / 2
+    rng = np.random.default_rng(51)
+    rand = np.ldexp(rng.uniform(1, 2, 3000), rng.integers(-12, 9, 3000))
+    ys = np.concatenate([vals, mids, -mids, rand[rand <= 448], -rand[rand <= 448]])
+    want = torch.from_numpy(ys).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.e4m3_encode(y) for y in ys], dtype=np.uint8)
+    same = (got == want) | ((got & 0x7F) == 0) & ((want & 0x7F) == 0)   # signed zeros
+    assert np.all(same), (ys[~same][:5], got[~same][:5], want[~same][:5])
+
+
+def check_kv_insert_latent(orc):
+    """The latent codes and scale bytes equal the generator's independent encoder; with the
+    identity rotation the rope bytes are the input BF16 bits; the padding is zero; the decoded
+    latent is within half an E4M3 step of the input."""
+    rng = np.random.default_rng(53)
+    T = 40
+    lat = rng.standard_normal((T, 512)) * np.ldexp(1.0, rng.integers(-30, 30, (T, 1)))
+    lat[0] = 0.0
+    lat[1, :128] = 448.0
+    rope = rng.standard_normal((T, 64))
+    kv = np.concatenate([_bf16(lat), _bf16(rope)], axis=1)
+    cache = np.full((T + 3, 656), 0xAB, dtype=np.uint8)
+    slots = np.arange(T, dtype=np.int64) + 2
+    out, bad = orc.kv_insert(kv, slots, np.zeros(T, np.int64), _rope_table(np.zeros((1, 32))), cache)
+    assert bad == 0
+    want = synth.quantize_entries(_from_bf16(kv[:, :512]), _from_bf16(kv[:, 512:]))
+    assert np.array_equal(out[2:T + 2], want)
+    assert np.all(out[:2] == 0xAB) and np.all(out[T + 2:] == 0xAB)
+    for t in range(T):
+        k = orc.dequant_entry(out[2 + t])[:512]
+        x = _from_bf16(kv[t, :512])
+        step = np.ldexp(1.0, int(out[2 + t, 640 + 0]) - 127)   # block 0's scale
+        assert np.all(np.abs(k[:128] - x[:128]) <= step * 32 + 1e-300)   # within half a step of 2^(e-127) * 64
+
+
+def check_rope_closed_forms(orc):
+    """GPT-J pairs: a rotation by 90 degrees maps (x, y) to (-y, x) exactly; a vector with one
+    nonzero rope dim 512 + 2i keeps its energy in dims 512 + 2i and 513 + 2i; pair norms are kept."""
+    rng = np.random.default_rng(57)
+    T = 6
+    lat = rng.standard_normal((T, 512))
+    rope = rng.standard_normal((T, 64))
+    kv = np.concatenate([_bf16(lat), _bf16(rope)], axis=1)
+    table = _rope_table(np.stack([np.full(32, np.pi / 2), rng.uniform(0, 6.3, 32)]))
+    table[0, :32] = 0.0   # exact cos 0
+    table[0, 32:] = 1.0   # exact sin 1
+    cache = np.zeros((T, 656), dtype=np.uint8)
+    out, _ = orc.kv_insert(kv, np.arange(T), np.zeros(T, np.int64), table, cache)
+    r = _from_bf16(out[:, 512:640].copy().view("<u2"))
+    x = _from_bf16(kv[:, 512:])
+    assert np.array_equal(r[:, 0::2], -x[:, 1::2]) and np.array_equal(r[:, 1::2], x[:, 0::2])
+    one = np.zeros((1, 576), dtype=np.uint16)
+    one[0, 512 + 6] = _bf16([1.0])[0]
+    out1, _ = orc.kv_insert(one, [0], [1], table, np.zeros((1, 656), np.uint8))
+    r1 = _from_bf16(out1[0, 512:640].copy().view("<u2"))
+    nz = set(np.nonzero(r1)[0].tolist())
+    assert nz <= {6, 7} and 6 in nz, nz
+    out2, _ = orc.kv_insert(kv, np.arange(T), np.ones(T, np.int64), table, cache)
+    r2 = _from_bf16(out2[:, 512:640].copy().view("<u2"))
+    n_in = x[:, 0::2] ** 2 + x[:, 1::2] ** 2
+    n_out = r2[:, 0::2] ** 2 + r2[:, 1::2] ** 2
+    assert np.allclose(n_in, n_out, rtol=2 ** -6, atol=1e-6)
+
+
+def check_qnorm_closed_forms(orc):
+    """A constant head c gives sign(c) / sqrt(1 + eps / c^2) in every dim (also at c = 2^-10, where
+    eps matters); the output's mean square is ms / (ms + eps); a weight of 2 doubles the output
+    exactly; a head whose only nonzero dims are rope dims is divided by sqrt(sum / 576) (the mean
+    runs over all 576 dims); zero stays zero."""
+    eps = 1e-6
+    ident = _rope_table(np.zeros((1, 32)))
+    qs = np.zeros((1, 1, 576), dtype=np.uint16)
+    qs[0, 0] = _bf16(np.full(576, 2.0 ** -10))
+    ys = _from_bf16(orc.qnorm_rope(qs, [0], ident, None, eps)[0])
+    want_s = 2.0 ** -10 / np.sqrt(2.0 ** -20 + eps)
+    assert np.all(np.abs(ys - want_s) <= want_s * 2 ** -8), (ys[0, 0, 0], want_s)
+    q = np.zeros((1, 4, 576), dtype=np.uint16)
+    q[0, 0] = _bf16(np.full(576, -3.0))
+    q[0, 1] = _bf16(np.random.default_rng(59).standard_normal(576))
+    q[0, 2, 512:] = _bf16(np.full(64, 2.0))
+    out, bad = orc.qnorm_rope(q, [0], ident, None, eps)
+    assert bad == 0
+    y = _from_bf16(out)
+    assert np.all(y[0, 0] == _from_bf16(_bf16([-1.0 / np.sqrt(1 + eps / 9.0)]))[0])
+    x1 = _from_bf16(q[0, 1])
+    ms = np.mean(x1 ** 2)
+    assert abs(np.mean(y[0, 1] ** 2) - ms / (ms + eps)) < 2 ** -7
+    want2 = 2.0 / np.sqrt(64 * 4.0 / 576 + eps)
+    assert np.all(y[0, 2, :512] == 0) and np.all(np.abs(y[0, 2, 512:] - want2) <= want2 * 2 ** -8)
+    assert np.all(y[0, 3] == 0)
+    out_w, _ = orc.qnorm_rope(q, [0], ident, np.full(576, 2.0, np.float32), eps)
+    assert np.array_equal(_from_bf16(out_w), 2 * y)
+
+
+def check_insert_slots_and_positions(orc):
+    """A negative slot writes nothing and is not counted; a slot past the cache or a position
+    outside the table writes nothing and is counted; such a query is normalised, not rotated."""
+    rng = np.random.default_rng(61)
+    kv = _bf16(rng.standard_normal((4, 576)))
+    table = _rope_table(rng.uniform(0, 6, (3, 32)))
+    cache = np.full((5, 656), 7, dtype=np.uint8)
+    out, bad = orc.kv_insert(kv, [-1, 5, 2, 1], [0, 1, 3, 2], table, cache)
+    assert bad == 2
+    assert np.all(out[[0, 2, 3, 4]] == 7) and not np.all(out[1] == 7)
+    q = _bf16(rng.standard_normal((2, 1, 576))).reshape(2, 1, 576)
+    qo, qbad = orc.qnorm_rope(q, [-4, 2], table)
+    assert qbad == 1
+    qi, _ = orc.qnorm_rope(q, [0, 2], _rope_table(np.zeros((3, 32))))
+    assert np.array_equal(qo[0], qi[0]) and not np.array_equal(qo[1], qi[1])
+
+
 ALL_CHECKS = [check_e4m3_codes, check_ue8m0, check_bf16, check_entry_layout, check_quantize_roundtrip,
               check_combine_golden, check_combine_bruteforce, check_combine_config1_lengths,
               check_dense_equivalence, check_order_padding_invariance, check_page_permutation, check_closed_forms,
               check_lse_identity_and_sink_limit, check_merge_partition, check_empty_and_bad_index,
               check_topk_lens_truncation, check_combine_compressed_golden, check_combine_compressed_invariants,
-              check_topk_golden, check_topk_distinct_vs_argpartition, check_topk_invariants]
+              check_topk_golden, check_topk_distinct_vs_argpartition, check_topk_invariants,
+              check_e4m3_encode, check_kv_insert_latent, check_rope_closed_forms, check_qnorm_closed_forms,
+              check_insert_slots_and_positions]

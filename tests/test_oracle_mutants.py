@@ -59,6 +59,19 @@ MUTANTS = [
     ("top-k: -0 below +0", "items[p].v = items[p].nan ? 0.0 : (double)x + 0.0;",
      "items[p].v = items[p].nan ? 0.0 : (signbit(x) && x == 0.0f ? -1e-300 : (double)x);"),
     ("top-k: length not capped by K", "topk_lens[t] = (int32_t)m;", "topk_lens[t] = (int32_t)n;"),
+    ("q norm: mean over the latent only", "const double r = 1.0 / sqrt(ss / OR_DIM + eps);",
+     "const double r = 1.0 / sqrt(ss / OR_LATENT + eps);"),
+    ("q norm: eps outside the root", "const double r = 1.0 / sqrt(ss / OR_DIM + eps);",
+     "const double r = 1.0 / (sqrt(ss / OR_DIM) + eps);"),
+    ("q norm: weight ignored", "x[d] = x[d] * r * (norm_w ? (double)norm_w[d] : 1.0);", "x[d] = x[d] * r;"),
+    ("rope: sine sign flipped", "*x = a * c - b * s;", "*x = a * c + b * s;"),
+    ("rope: NeoX pairs in the key", ("rope_pair(&x[OR_LATENT + 2 * i], &x[OR_LATENT + 2 * i + 1], (double)cos_sin[pos * 64 + i],\n                      (double)cos_sin[pos * 64 + 32 + i]);\n        for (int i = 0; i < OR_ROPE; ++i)",),
+     ("rope_pair(&x[OR_LATENT + i], &x[OR_LATENT + i + 32], (double)cos_sin[pos * 64 + i],\n                      (double)cos_sin[pos * 64 + 32 + i]);\n        for (int i = 0; i < OR_ROPE; ++i)",)),
+    ("insert: scale byte off by one", "e[OR_SCALE_OFF + b] = (uint8_t)(ex + 127);", "e[OR_SCALE_OFF + b] = (uint8_t)(ex + 128);"),
+    ("insert: codes rounded toward zero", "int q = (int)rint((2.0 * m - 1.0) * 8.0);", "int q = (int)floor((2.0 * m - 1.0) * 8.0);"),
+    ("insert: scale exponent one high", "while (e < 127 && 448.0 * ldexp(1.0, e) < amax)", "while (e < 127 && 448.0 * ldexp(1.0, e) <= amax)"),
+    ("insert: negative slot counted as bad", "if (slot < 0)\n            continue;\n        if (slot >= num_slots",
+     "if (slot < 0) {\n            ++bad;\n            continue;\n        }\n        if (slot >= num_slots"),
 ]
 
 
