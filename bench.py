@@ -60,8 +60,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["decode", "combine-compressed", "topk-select"], default="decode",
-                    help="decode (the headline), or the compressed-region combine or the top-k selection on its own")
+    ap.add_argument("--op", choices=["decode", "combine-compressed", "topk-select", "qnorm-rope-insert"],
+                    default="decode", help="decode (the headline), or one of the steps around it on its own")
     ap.add_argument("--topk-workload", choices=["long-batch", "long-decode"], default="long-batch",
                     help="top-k selection workload (synth.topk_config)")
     ap.add_argument("--replicas", type=int, default=0,
@@ -668,8 +668,101 @@ def run_topk_select(args):
     return 0
 
 
+def run_qnorm_rope_insert(args):
+    """The fused query RMSNorm + GPT-J RoPE + FP8 KV insert on its own: 128 tokens x 128 heads
+    (the long-context decode's shape), positions below 32768, distinct slots in a 65536-slot
+    cache. Bytes per step: queries read and written (2 * T * H * 1152), keys read (T * 1152),
+    entries written (T * 656), cos/sin rows, positions and slots read (T * 272)."""
+    import torch
+    import synth
+    import sparse_mla_decode_combine_gb300 as pkg
+    from sparse_mla_decode_combine_gb300 import build as pkg_build
+    pkg_build.build()
+    pkg.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rng = np.random.default_rng(7)
+    T, H, P, S = 128, 128, 32768, 65536
+    bytes_per_step = 2 * T * H * 1152 + T * 1152 + T * 656 + T * 272
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    reps = args.replicas if args.replicas > 0 else max(2, math.ceil(4 * l2 / bytes_per_step))
+    q0 = torch.from_numpy(synth.bf16_bits(rng.standard_normal((T, H, 576))).view(np.int16)).view(torch.bfloat16).to(dev)
+    kv0 = torch.from_numpy(synth.bf16_bits(rng.standard_normal((T, 576))).view(np.int16)).view(torch.bfloat16).to(dev)
+    qs = [q0.clone() for _ in range(reps)]
+    qo = [torch.empty_like(q0) for _ in range(reps)]
+    kvs = [kv0.clone() for _ in range(reps)]
+    ang = rng.uniform(0, 2 * np.pi, (P, 32))
+    table = torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)).to(dev)
+    pos = torch.from_numpy(rng.integers(0, P, T).astype(np.int64)).to(dev)
+    slots = torch.from_numpy(rng.permutation(S)[:T].astype(np.int64)).to(dev)
+    cache = torch.zeros((S, 656), dtype=torch.uint8, device=dev)
+    w = torch.from_numpy(rng.uniform(0.5, 1.5, 576).astype(np.float32)).to(dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        r = i % reps
+        pkg.check(pkg.dsv4_qnorm_rope_kv_insert(qs[r], qo[r], kvs[r], pos, slots, table, cache, w, 1e-6,
+                                                stream=stream))
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            step(i)
+    torch.cuda.synchronize()
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        return g
+    graph = capture(reps)
+    replays, rem = divmod(max(args.steps, 1), reps)
+    tail = capture(rem) if rem else None
+    torch.cuda.synchronize()
+    steps = replays * reps + rem
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    sampler.start()
+    time.sleep(0.2)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        if tail is not None:
+            tail.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    step_s = ms / 1e3 / steps
+    hbm_peak, _, _, peak_src = peaks()
+    ach = bytes_per_step / step_s / 1e9
+    line = {"metric": "fused q-norm/RoPE/KV-insert query-tokens/s (bytes moved vs HBM roofline)",
+            "value": T / step_s, "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "q RMSNorm + GPT-J RoPE + FP8 KV insert: 128 tokens x 128 heads, 65536-slot cache",
+                       "tokens_per_step": T, "heads": H, "replicas": reps,
+                       "l2": f"inputs larger than L2: {reps} rotating replicas"},
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                         "traffic": None, "kernel": "qnorm_rope_kv_insert_kernel",
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+                         "algorithmic_bytes_per_launch": bytes_per_step,
+                         "timed": "one call (one launch) per step, CUDA events on the launching stream"},
+            "gpu_launches": steps, "launches_per_step": 1, "clocks": sampler.summary(t0, t1)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.op == "qnorm-rope-insert":
+        if args.impl == "reference" or int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        return run_qnorm_rope_insert(args)
     if args.op == "topk-select":
         if args.impl == "reference" or int(os.environ.get("RANK", "0")) != 0:
             return 0

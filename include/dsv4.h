@@ -154,6 +154,44 @@ DSV4_API dsv4_status dsv4_combine_topk_swa_indices_compressed(
     int64_t combined_stride, int32_t combined_width, int32_t *combined_lens, dsv4_stream_t stream);
 
 /*
+ * dsv4_qnorm_rope_kv_insert -- the step before the decode: normalise and rotate the queries and
+ * write each token's key into the FP8 cache.
+ *
+ * Source: vllm #42953 "feat: add DeepSeek-V4 XPU attention decode path", section 实现拆解 4
+ * (xpu_qnorm_rope_kv_fp8_insert: fused Q per-head RMSNorm, GPT-J RoPE and FP8 UE8M0 KV insert,
+ * called from forward_mqa with q, kv, kv_cache, slot_mapping and positions).  The page names
+ * the steps, not their formulas; this library's readings:
+ *   q_out[t][h] = RoPE(q[t][h] / sqrt(mean over 576 dims of q[t][h]^2 + eps) * w)
+ *   kv_cache[slot_mapping[t]] = entry(kv[t]): per 128 latent values the smallest e with
+ *       448 * 2^e >= amax (0 for amax 0, clamped to [-127, 127]), E4M3 codes of x * 2^-e
+ *       (nearest, ties to even), scale byte e + 127; the rotated rope part in BF16; zero padding
+ * GPT-J RoPE rotates the interleaved pairs (512 + 2i, 513 + 2i), i < 32, by the angle whose
+ * cosine and sine are cos_sin_cache[positions[t]][i] and [32 + i].  The arithmetic is fp32 with
+ * one rounding to BF16 (queries) or E4M3/BF16 (entries) at the end.
+ *
+ * Arguments:
+ *   q, q_out         BF16 [num_tokens, num_heads, 576], token strides in elements (even, >=
+ *                    num_heads * 576); q_out may be q.  Both 4-byte aligned.
+ *   num_heads        1..128; q_norm_weight fp32 [576] or NULL (all ones); eps >= 0.
+ *   kv               BF16 [num_tokens, 576] (512 latent, then 64 rope), token stride even, >= 576.
+ *   positions, slot_mapping  int64 [num_tokens].
+ *   cos_sin_cache    fp32 [max_position, 64]: 32 cosines, then 32 sines per position.
+ *   kv_cache         uint8 [num_slots, 656] (a paged cache [num_blocks, page, 656] has
+ *                    num_blocks * page slots), 16-byte aligned.
+ * A negative slot writes nothing (a padding token).  A slot >= num_slots, or a position outside
+ * [0, max_position), writes no entry and sets DSV4_ERR_BAD_INDEX in the device status word; such
+ * a token's query is normalised but not rotated.  Nothing is allocated.  Returns DSV4_OK,
+ * DSV4_ERR_INVALID_ARG or DSV4_ERR_CUDA.
+ */
+DSV4_API dsv4_status dsv4_qnorm_rope_kv_insert(const void *q, int64_t q_token_stride, void *q_out,
+                                               int64_t q_out_token_stride, int32_t num_tokens, int32_t num_heads,
+                                               const float *q_norm_weight, float eps, const void *kv,
+                                               int64_t kv_token_stride, const int64_t *positions,
+                                               const int64_t *slot_mapping, const float *cos_sin_cache,
+                                               int32_t max_position, void *kv_cache, int64_t num_slots,
+                                               dsv4_stream_t stream);
+
+/*
  * dsv4_topk_select -- each token's top-k row from its indexer scores (the step that produces
  * topk_idx for the decode).
  *

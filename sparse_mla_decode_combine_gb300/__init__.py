@@ -30,6 +30,7 @@ STATUS_NAMES = {0: "DSV4_OK", 1: "DSV4_ERR_INVALID_ARG", 2: "DSV4_ERR_BAD_INDEX"
                 4: "DSV4_ERR_CUDA", 5: "DSV4_ERR_UNSUPPORTED"}
 
 EXPORTED = ("dsv4_combine_topk_swa_indices", "dsv4_combine_topk_swa_indices_compressed", "dsv4_topk_select",
+            "dsv4_qnorm_rope_kv_insert",
             "dsv4_sparse_mla_decode_workspace_size", "dsv4_sparse_mla_decode", "dsv4_sparse_mla_decode_noalloc",
             "dsv4_get_device_status")
 
@@ -67,6 +68,9 @@ def load_library():
     lib.dsv4_combine_topk_swa_indices_compressed.restype = ctypes.c_int
     lib.dsv4_combine_topk_swa_indices_compressed.argtypes = [P, i64, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                              P, i64, i32, P, P]
+    lib.dsv4_qnorm_rope_kv_insert.restype = ctypes.c_int
+    lib.dsv4_qnorm_rope_kv_insert.argtypes = [P, i64, P, i64, i32, i32, P, ctypes.c_float, P, i64, P, P, P, i32, P,
+                                              i64, P]
     lib.dsv4_topk_select.restype = ctypes.c_int
     lib.dsv4_topk_select.argtypes = [P, i64, i32, P, i32, i32, P, i64, P, P]
     lib.dsv4_sparse_mla_decode_workspace_size.restype = ctypes.c_size_t
@@ -141,6 +145,32 @@ def dsv4_combine_topk_swa_indices_compressed(topk_idx: torch.Tensor, query_start
         _ptr(gather_lens), query_start_loc.numel() - 1, T, int(region_stride), int(compressed_len), int(top_k),
         int(compress_ratio), int(window), _ptr(combined), max(combined.stride(0), combined.shape[1]),
         combined.shape[1], _ptr(combined_lens), _stream(stream))
+
+
+def dsv4_qnorm_rope_kv_insert(q: torch.Tensor, q_out: torch.Tensor, kv: torch.Tensor, positions: torch.Tensor,
+                              slot_mapping: torch.Tensor, cos_sin_cache: torch.Tensor, kv_cache: torch.Tensor,
+                              q_norm_weight: Optional[torch.Tensor] = None, eps: float = 1e-6, stream=None) -> int:
+    """q, q_out bf16 [T, H, 576] (heads contiguous); kv bf16 [T, 576]; positions, slot_mapping int64 [T];
+    cos_sin_cache float32 [max_position, 64]; kv_cache uint8 [..., 656] (slots in order);
+    q_norm_weight float32 [576] or None."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(q_out, torch.bfloat16, "q_out", 3)
+    _need(kv, torch.bfloat16, "kv", 2)
+    _need(positions, torch.int64, "positions", 1)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(cos_sin_cache, torch.float32, "cos_sin_cache", 2)
+    _need(kv_cache, torch.uint8, "kv_cache")
+    _need(q_norm_weight, torch.float32, "q_norm_weight", 1)
+    T, H, _ = q.shape
+    if q.stride(1) != 576 or q_out.stride(1) != 576:
+        raise ValueError("q, q_out: heads must be contiguous")
+    if not kv_cache.is_contiguous():
+        raise ValueError("kv_cache: must be contiguous")
+    return load_library().dsv4_qnorm_rope_kv_insert(
+        _ptr(q), q.stride(0), _ptr(q_out), q_out.stride(0), T, H,
+        _ptr(q_norm_weight) if q_norm_weight is not None else None, float(eps), _ptr(kv), kv.stride(0),
+        _ptr(positions), _ptr(slot_mapping), _ptr(cos_sin_cache), cos_sin_cache.shape[0], _ptr(kv_cache),
+        kv_cache.numel() // 656, _stream(stream))
 
 
 def dsv4_topk_select(scores: torch.Tensor, num_cand: torch.Tensor, top_k: int, topk_idx: torch.Tensor,

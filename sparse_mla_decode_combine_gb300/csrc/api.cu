@@ -236,6 +236,34 @@ extern "C" DSV4_API dsv4_status dsv4_combine_topk_swa_indices_compressed(
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
+extern "C" DSV4_API dsv4_status dsv4_qnorm_rope_kv_insert(
+    const void *q, int64_t q_token_stride, void *q_out, int64_t q_out_token_stride, int32_t num_tokens,
+    int32_t num_heads, const float *q_norm_weight, float eps, const void *kv, int64_t kv_token_stride,
+    const int64_t *positions, const int64_t *slot_mapping, const float *cos_sin_cache, int32_t max_position,
+    void *kv_cache, int64_t num_slots, dsv4_stream_t stream)
+{
+    if (num_tokens < 0 || num_heads < 1 || num_heads > 128 || !(eps >= 0.f) || !std::isfinite(eps) ||
+        max_position < 1 || num_slots < 0)
+        return DSV4_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return DSV4_OK;
+    const int64_t row = (int64_t)num_heads * kDim;
+    auto odd = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) != 0; };
+    if (q == nullptr || q_out == nullptr || kv == nullptr || positions == nullptr || slot_mapping == nullptr ||
+        cos_sin_cache == nullptr || (num_slots > 0 && kv_cache == nullptr) || q_token_stride < row ||
+        q_out_token_stride < row || kv_token_stride < kDim || (q_token_stride | q_out_token_stride | kv_token_stride) & 1 ||
+        odd(q) || odd(q_out) || odd(kv) || (num_slots > 0 && (reinterpret_cast<uintptr_t>(kv_cache) & 15u) != 0))
+        return DSV4_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    if (device_info(&status, nullptr) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    cudaError_t e = launch_qnorm_rope_kv_insert(q, q_token_stride, q_out, q_out_token_stride, num_tokens, num_heads,
+                                                q_norm_weight, eps, kv, kv_token_stride, positions, slot_mapping,
+                                                cos_sin_cache, max_position, kv_cache, num_slots, status,
+                                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
 extern "C" DSV4_API dsv4_status dsv4_topk_select(const float *scores, int64_t score_stride, int32_t score_width,
                                                  const int32_t *num_cand, int32_t num_tokens, int32_t top_k,
                                                  int32_t *topk_idx, int64_t topk_stride, int32_t *topk_lens,

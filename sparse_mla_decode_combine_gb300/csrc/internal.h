@@ -103,6 +103,13 @@ cudaError_t launch_combine_compressed(const int32_t *topk, int64_t topk_stride, 
 cudaError_t launch_after_previous(const void *kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
                                   const DecodeParams &p);
 
+// Fused Q RMSNorm + GPT-J RoPE + FP8/UE8M0 KV-cache insert (strides in BF16 elements, even).
+cudaError_t launch_qnorm_rope_kv_insert(const void *q, int64_t q_stride, void *q_out, int64_t q_out_stride,
+                                        int num_tokens, int num_heads, const float *norm_w, float eps,
+                                        const void *kv, int64_t kv_stride, const int64_t *positions,
+                                        const int64_t *slots, const float *cos_sin, int max_pos, void *cache,
+                                        int64_t num_slots, unsigned *status, cudaStream_t stream);
+
 // Top-k selection: CTAs per token row (a thread-block cluster when > 1), and the launch.
 int topk_cluster_size(int num_tokens, int width, int sms);
 cudaError_t launch_topk_select(const float *scores, int64_t score_stride, int width, const int32_t *num_cand,

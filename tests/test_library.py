@@ -73,6 +73,17 @@ def test_host_side_argument_errors(lib):
     assert tk(P, 16, 16, P, 1, 4, P, 3, None, S) == pkg.DSV4_ERR_INVALID_ARG
     assert tk(P, 8, 16, P, 1, 4, P, 4, None, S) == pkg.DSV4_ERR_INVALID_ARG
     assert tk(None, 0, 0, None, 0, 4, None, 0, None, S) == pkg.DSV4_OK
+    # fused norm/RoPE/insert: heads 0 and 129, NaN eps, odd stride, nothing to do
+    ins = lib.dsv4_qnorm_rope_kv_insert
+    #         q, qs,   qo, qos,  T, H,  w,    eps,  kv, kvs, pos, slot, cs, maxp, cache, nslots, stream
+    good = [P, 1152, P, 1152, 1, 2, None, 1e-6, P, 576, P, P, P, 8, P, 4, S]
+    for i, v in ((5, 0), (5, 129), (7, float("nan")), (1, 1153), (9, 577), (13, 0)):
+        bad = list(good)
+        bad[i] = v
+        assert ins(*bad) == pkg.DSV4_ERR_INVALID_ARG, (i, v)
+    bad = list(good)
+    bad[4] = 0
+    assert ins(*bad) == pkg.DSV4_OK
     # decode: unsupported head count, non-finite scale, missing pointers
     args = [None, 576 * 16, None, 1, 64, None, 1, 1, 1, None, None, 0, 0, None, ctypes.c_void_p(16), 1, 16, 8, None,
             1.0, None, None, None, 0, S]
