@@ -119,6 +119,33 @@ def test_decode_junk_topk_entries(heads):
     compare_decode(out, lse, ref_out, ref_lse, what=f"junk top-k h={heads}")
 
 
+@pytest.mark.parametrize("heads", [64, 128])
+def test_decode_max_topk_width(heads):
+    """The widest top-k rows the library takes (8192 entries, the fused combine's hash set at its
+    2^14-slot cap and half full) with a 1024-entry window: many repeats of a few thousand
+    positions, -1 padding, positions past the token and inside the window."""
+    need_gpu()
+    rng = np.random.default_rng(47)
+    K = 8192
+    w = synth.make_workload(name="widest", seed=49, heads=heads, req_seq_lens=[40000, 12000, 9000],
+                            topk_width=K, window=1024, sink=True)
+    topk = w.topk_idx.copy()
+    for t in range(w.num_tokens):
+        pos = int(w.seq_lens[t]) - 1
+        row = topk[t]
+        m = rng.random(K)
+        pool = rng.integers(0, pos + 1, size=3000)
+        row[m < 0.5] = pool[rng.integers(0, 3000, size=int((m < 0.5).sum()))]   # repeats of 3000 positions
+        row[(m >= 0.5) & (m < 0.6)] = -1
+        row[(m >= 0.6) & (m < 0.65)] = pos + 1 + rng.integers(0, 50, size=int(((m >= 0.6) & (m < 0.65)).sum()))
+        row[(m >= 0.65) & (m < 0.7)] = pos - rng.integers(0, 1024, size=int(((m >= 0.65) & (m < 0.7)).sum()))
+    w = synth.Workload(**{**w.__dict__, "topk_idx": topk, "topk_lens": None})
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(w)
+    compare_decode(out, lse, ref_out, ref_lse, what=f"widest top-k h={heads}")
+
+
 def test_decode_window_only_and_topk_only():
     need_gpu()
     w = small(5)
