@@ -10,9 +10,9 @@
 // GPU), each CTA a contiguous segment of the row.  Scores become order-preserving 32-bit
 // keys; three histogram rounds (11, 11 and 10 bits from the top) find the K-th largest key
 // v* and how many keys equal to v* the selection takes.  For each round every CTA builds its
-// segment's histogram in shared memory and reduces one slice of the bins across the cluster
-// through distributed shared memory; the owner of the slice holding the K-th key broadcasts
-// the digit.  Round 0 reads the scores from HBM with 16-byte loads issued four deep and keeps
+// segment's histogram in shared memory, sums one slice of the bins over the cluster through
+// distributed shared memory and writes the sums into every CTA; each CTA then finds the digit
+// itself (two cluster barriers a round).  Round 0 reads the scores from HBM with 16-byte loads issued four deep and keeps
 // the segment's keys in shared memory (up to 40960 keys a CTA).  One pass over the cached
 // keys then lists the keys of round 0's bin with their positions (up to 256 a warp chunk) and
 // counts the keys above it; rounds 1 and 2 and the per-chunk counts work on that list alone
@@ -218,8 +218,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     constexpr int kTkWarps = NT / 32;
     constexpr int kTkCandWarp = kTkCandMax / kTkWarps;   // a sub-list per warp chunk
     __shared__ uint32_t hist[kTkBins];     // this CTA's histogram of the round
-    __shared__ uint32_t slice[kTkBins];    // this CTA's slice of the cluster-wide histogram
-    __shared__ uint32_t sums[8];           // slice totals of every CTA of the cluster
+    __shared__ uint32_t slice[kTkBins];    // the cluster-wide histogram (clusters of more than one CTA)
     __shared__ uint32_t bcast[2];          // the round's digit and remaining count
     __shared__ uint32_t cnt[8][2];         // (> v*, == v*) counts per CTA
     __shared__ uint32_t wsum[kTkWarps];
@@ -282,13 +281,12 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     auto find_digit = [&](int nb) -> uint32_t {
         sync_all();   // every segment's histogram is complete
         const uint32_t *bins = hist;
-        int s_lo = 0, s_hi = nb, owner = 0;
-        uint32_t above = 0u;
-        if (CL > 1) {   // this CTA's slice of the bins, summed over the cluster
+        if (CL > 1) {
+            // this CTA sums its slice of the bins over the cluster and writes the sums into every
+            // CTA's copy of the cluster-wide histogram (`slice`)
             const int per = (nb + CL - 1) / CL;
-            s_lo = min(nb, (int)rank * per);
-            s_hi = min(nb, s_lo + per);
-            uint32_t part = 0u;
+            const int s_lo = min(nb, (int)rank * per);
+            const int s_hi = min(nb, s_lo + per);
             for (int b = s_lo + tid; b < s_hi; b += kTkThreads) {
                 uint32_t v[8];
 #pragma unroll
@@ -298,49 +296,33 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
 #pragma unroll
                 for (int r = 0; r < 8; ++r)
                     sm += v[r];
-                slice[b - s_lo] = sm;
-                part += sm;
+                for (int r = 0; r < CL; ++r)
+                    put(&slice[b], r, sm);
             }
-            uint32_t tot;
-            block_scan<NT>(part, wsum, tot);
-            if (tid < CL)
-                put(&sums[rank], tid, tot);
-            cluster_barrier();   // slice totals everywhere
-            for (int r = CL - 1; r >= 0; --r) {   // higher ranks hold higher bins
-                if (above + sums[r] >= rem) {
-                    owner = r;
-                    break;
-                }
-                above += sums[r];
-            }
+            cluster_barrier();   // the cluster-wide histogram is in every CTA; remote reads of hist are over
             bins = slice;
         }
-        if ((int)rank == owner) {
-            // thread i takes the i-th group of c bins counted from the top of the slice
-            const int nbs = s_hi - s_lo;
-            const int c = (nbs + kTkThreads - 1) / kTkThreads;
-            const int g_hi = nbs - tid * c;
-            const int g_lo = max(0, g_hi - c);
-            uint32_t gs = 0u;
-            for (int b = g_lo; b < g_hi; ++b)
-                gs += bins[b];
-            uint32_t gtot;
-            const uint32_t incl = block_scan<NT>(gs, wsum, gtot);
-            uint32_t a = above + incl - gs;   // keys in bins above this group
-            if (g_lo < g_hi && a < rem && rem <= a + gs) {
-                for (int b = g_hi - 1; b >= g_lo; --b) {
-                    if (a + bins[b] >= rem) {
-                        for (int r = 0; r < CL; ++r) {
-                            put(&bcast[0], r, (uint32_t)(s_lo + b));
-                            put(&bcast[1], r, rem - a);
-                        }
-                        break;
-                    }
-                    a += bins[b];
+        // every CTA finds the digit itself: thread i takes the i-th group of c bins from the top
+        const int c = (nb + kTkThreads - 1) / kTkThreads;
+        const int g_hi = nb - tid * c;
+        const int g_lo = max(0, g_hi - c);
+        uint32_t gs = 0u;
+        for (int b = g_lo; b < g_hi; ++b)
+            gs += bins[b];
+        uint32_t gtot;
+        const uint32_t incl = block_scan<NT>(gs, wsum, gtot);
+        uint32_t a = incl - gs;   // keys in bins above this group
+        if (g_lo < g_hi && a < rem && rem <= a + gs) {
+            for (int b = g_hi - 1; b >= g_lo; --b) {
+                if (a + bins[b] >= rem) {
+                    bcast[0] = (uint32_t)b;
+                    bcast[1] = rem - a;
+                    break;
                 }
+                a += bins[b];
             }
         }
-        sync_all();   // the digit is known everywhere; remote reads of hist are over
+        __syncthreads();
         rem = bcast[1];
         return bcast[0];
     };
