@@ -14,8 +14,14 @@ outputs) so the bytes the timed steps gather exceed 4x the L2; CUDA events on
 the launching stream, barrier + synchronize on both sides, max over ranks.
 The roofline divides the algorithmic bytes (or FLOPs) of a step by the CUDA-event
 time of the whole decode call; per-kernel shares come from the committed ncu launch
-list (CUPTI kernel records are not available on the GPU machines).  e2e repeats the step through the same C ABI
-from pinned host buffers with the host<->device copies inside the timed region.
+list (CUPTI kernel records are not available on the GPU machines).  e2e repeats the step through
+the same C ABI with every step's host<->device copies inside the timed region: one packed upload
+of the inputs from pinned memory and one read-back of the output and LSE per step, on copy
+streams double-buffered against the calls (as a serving loop overlaps them), 64 steps a graph.
+
+Other ops, timed the same way on their own workloads: --op topk-select (top-k selection from
+indexer scores), --op combine-compressed (the compressed-region combine), --op
+qnorm-rope-insert (fused query norm/RoPE and FP8 KV insert).
 N > 1: every rank decodes its own batch on its own GPU (no data-path
 collective; weak scaling).
 
