@@ -14,7 +14,7 @@
 // distributed shared memory and writes the sums into every CTA; each CTA then finds the digit
 // itself (two cluster barriers a round).  Round 0 reads the scores from HBM with 16-byte loads issued four deep and keeps
 // the segment's keys in shared memory (up to 40960 keys a CTA).  One pass over the cached
-// keys then lists the keys of round 0's bin with their positions (up to 256 a warp chunk) and
+// keys then lists the keys of round 0's bin with their positions (up to 128 a warp chunk) and
 // counts the keys above it; rounds 1 and 2 and the per-chunk counts work on that list alone
 // (a segment with more candidates, i.e. many equal keys, rescans its keys instead).  The
 // compaction walks the segment in position order, one contiguous chunk per warp with warp
@@ -34,7 +34,7 @@ constexpr int kTkThreadsCluster = 512;
 constexpr int kTkBins = 2048;          // 11-bit digits
 constexpr int kTkCacheKeys = 40960;    // keys of a segment kept in shared memory (160 KB)
 constexpr int kTkStep = 32 * 8;        // compaction: a warp takes 8 consecutive positions per lane
-constexpr int kTkCandMax = 4096;       // candidates (keys in round 0's bin) kept in shared memory
+constexpr int kTkCandWarp = 128;       // candidates (keys in round 0's bin) a warp chunk keeps in shared memory
 
 struct TopkParams {
     const float *scores;
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
 {
     constexpr int kTkThreads = NT;
     constexpr int kTkWarps = NT / 32;
-    constexpr int kTkCandWarp = kTkCandMax / kTkWarps;   // a sub-list per warp chunk
+    constexpr int kTkCandMax = kTkCandWarp * kTkWarps;
     __shared__ uint32_t hist[kTkBins];     // this CTA's histogram of the round
     __shared__ uint32_t slice[kTkBins];    // the cluster-wide histogram (clusters of more than one CTA)
     __shared__ uint32_t bcast[2];          // the round's digit and remaining count
@@ -225,10 +225,12 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     __shared__ uint32_t wsure[kTkWarps];     // keys above round 0's bin per warp chunk
     __shared__ uint32_t wcnt[kTkWarps][2];   // (> v*, == v*) counts per warp chunk
     __shared__ uint32_t wncand[kTkWarps];    // candidates per warp chunk
-    extern __shared__ uint4 dyn4[];        // [p.cache keys][kTkCandMax candidate keys][kTkCandMax positions]
+    // [p.cache keys][kTkCandMax candidate keys][kTkCandMax positions][a bit per cached position]
+    extern __shared__ uint4 dyn4[];
     uint32_t *kc = reinterpret_cast<uint32_t *>(dyn4);
     uint32_t *ckey = kc + p.cache;
     uint32_t *cpos = ckey + kTkCandMax;
+    uint32_t *bm = cpos + kTkCandMax;      // the selected positions of the segment (with the cache)
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -269,8 +271,9 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
     const bool cache = p.cache > 0;
     const int len = (int)(hi - lo);
-    // warp w owns the chunk [c_lo, c_hi) of the segment (a multiple of 8 positions long)
-    const int cw = ((len + kTkWarps - 1) / kTkWarps + 7) / 8 * 8;
+    // warp w owns the chunk [c_lo, c_hi) of the segment (a multiple of 128 positions long, so that
+    // chunks start on a bitmap word)
+    const int cw = ((len + kTkWarps - 1) / kTkWarps + 127) / 128 * 128;
     const int c_lo = min(len, warp * cw);
     const int c_hi = min(len, c_lo + cw);
     auto key_at = [&](int i) -> uint32_t { return cache ? kc[i] : order_key(__ldg(row + lo + i)); };
@@ -330,18 +333,21 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     // ---- round 0 (top 11 bits) over every key; the keys go to the shared-memory cache
     for (int i = tid; i < kTkBins; i += kTkThreads)
         hist[i] = 0u;
+    if (cache)
+        for (int i = tid; i < (len + 31) / 32; i += kTkThreads)
+            bm[i] = 0u;
     __syncthreads();
     visit_keys<NT>(row, lo, hi, vec, kc, false, cache, [&](uint32_t k) { atomicAdd(&hist[k >> 21], 1u); });
     const uint32_t d0 = find_digit(kTkBins);
     uint32_t prefix = d0 << 21, pmask = 0xFFE00000u;
 
     // ---- the keys in round 0's bin become candidates (key, position), each warp listing those
-    // of its chunk; keys above the bin are selected whatever the later rounds find
+    // of its chunk in position order; keys above the bin are selected whatever the later rounds
+    // find: they are counted, and (with the cache) marked in the bitmap
     uint32_t sure = 0u, nw = 0u;   // per lane: keys above the bin; per warp: candidates so far
     uint32_t *wkey = ckey + warp * kTkCandWarp;
     uint32_t *wpos = cpos + warp * kTkCandWarp;
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int i0 = c_lo; i0 < c_hi; i0 += 128) {   // four consecutive keys a lane
+    for (int i0 = c_lo; i0 < c_hi; i0 += 128) {   // four consecutive keys a lane, 8 lanes a bitmap word
         const int i = i0 + 4 * lane;
         uint32_t k[4];
         if (cache && i + 4 <= c_hi) {
@@ -355,19 +361,38 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
             for (int j = 0; j < 4; ++j)
                 k[j] = i + j < c_hi ? key_at(i + j) : 0u;
         }
+        uint32_t bits = 0u, nc = 0u;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const bool in = i + j < c_hi;
-            sure += (in && (k[j] >> 21) > d0) ? 1u : 0u;
-            const bool cand = in && (k[j] >> 21) == d0;
-            const uint32_t bal = __ballot_sync(0xffffffffu, cand);
-            const uint32_t slot = nw + (uint32_t)__popc(bal & lt);
-            if (cand && slot < (uint32_t)kTkCandWarp) {
-                wkey[slot] = k[j];
-                wpos[slot] = (uint32_t)(i + j);
-            }
-            nw += (uint32_t)__popc(bal);
+            const bool up = in && (k[j] >> 21) > d0;
+            sure += up ? 1u : 0u;
+            bits |= up ? 1u << (4 * (lane & 7) + j) : 0u;
+            nc += (in && (k[j] >> 21) == d0) ? 1u : 0u;
         }
+        uint32_t incl = nc;   // candidates up to this lane's four keys, in position order
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        uint32_t slot = nw + incl - nc;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (i + j < c_hi && (k[j] >> 21) == d0) {
+                if (slot < (uint32_t)kTkCandWarp) {
+                    wkey[slot] = k[j];
+                    wpos[slot] = (uint32_t)(i + j);
+                }
+                ++slot;
+            }
+        nw += __shfl_sync(0xffffffffu, incl, 31);
+        bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
+        bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
+        bits |= __shfl_xor_sync(0xffffffffu, bits, 4);
+        if (cache && (lane & 7) == 0 && i < c_hi)
+            bm[i >> 5] = bits;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
@@ -462,6 +487,47 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
         E += cnt[r][1];
     }
 
+    if (listed && cache) {
+        // ---- the candidates above v*, and those equal to it that the budget reaches (in position
+        // order: the rank among equal keys before them in the row), join the bitmap
+        uint32_t eseen = E + we;
+        const uint32_t nwc = wncand[warp];
+        for (uint32_t b0 = 0; b0 < nwc; b0 += 32) {
+            const uint32_t c = b0 + lane;
+            const bool in = c < nwc;
+            const uint32_t k = in ? wkey[c] : 0u;
+            const bool gt = in && k > vstar;
+            const bool eq = in && k == vstar;
+            const uint32_t bal = __ballot_sync(0xffffffffu, eq);
+            const uint32_t rank = eseen + (uint32_t)__popc(bal & ((1u << lane) - 1u));
+            if (gt || (eq && rank < rem)) {
+                const uint32_t pos = wpos[c];
+                atomicOr(&bm[pos >> 5], 1u << (pos & 31));
+            }
+            eseen += (uint32_t)__popc(bal);
+        }
+        __syncthreads();
+        // ---- the bitmap in position order: thread t takes words [t q, t q + q)
+        const int words = (len + 31) / 32;
+        const int q = (words + kTkThreads - 1) / kTkThreads;
+        const int w_lo = min(words, tid * q);
+        const int w_hi = min(words, w_lo + q);
+        uint32_t nsel = 0u;
+        for (int wi = w_lo; wi < w_hi; ++wi)
+            nsel += (uint32_t)__popc(bm[wi]);
+        uint32_t stot;
+        uint32_t o = G + min(E, rem) + block_scan<NT>(nsel, wsum, stot) - nsel;
+        for (int wi = w_lo; wi < w_hi; ++wi) {
+            uint32_t x = bm[wi];
+            while (x != 0u) {
+                const int bit = __ffs(x) - 1;
+                orow[o++] = (int32_t)(lo + 32 * wi + bit);
+                x &= x - 1u;
+            }
+        }
+        return;
+    }
+
     // ---- position-ordered compaction over this warp's chunk: the output index of a selected
     // position is (keys > v* before it) + min(keys == v* before it, rem)
     uint32_t gb = G + wg, eb = E + we;   // keys > v* and == v* before this lane's next positions
@@ -531,10 +597,12 @@ cudaError_t launch_topk_select(const float *scores, int64_t score_stride, int wi
     // every segment's keys in shared memory when the longest segment fits the cache
     const long long seg_max = (((long long)width + cluster - 1) / cluster + 3) / 4 * 4;
     const int cache = seg_max <= kTkCacheKeys ? (int)seg_max : 0;
-    const int smem = 4 * cache + 8 * kTkCandMax;
+    const int warps = (cluster > 1 ? kTkThreadsCluster : kTkThreadsRow) / 32;
+    const int smem = 4 * cache + 8 * kTkCandWarp * warps + (cache ? 4 * ((cache + 31) / 32) : 0);
     const void *kernel = cluster > 1 ? reinterpret_cast<const void *>(topk_select_kernel<kTkThreadsCluster>)
                                      : reinterpret_cast<const void *>(topk_select_kernel<kTkThreadsRow>);
-    cudaError_t e = set_smem_once(kernel, 4 * kTkCacheKeys + 8 * kTkCandMax, cluster > 1 ? kAttrTopkCluster : kAttrTopk);
+    cudaError_t e = set_smem_once(kernel, 4 * kTkCacheKeys + 8 * kTkCandWarp * 32 + 4 * (kTkCacheKeys / 32),
+                                  cluster > 1 ? kAttrTopkCluster : kAttrTopk);
     if (e != cudaSuccess)
         return e;
     TopkParams p{scores, score_stride, width, num_cand, top_k, out, out_stride, lens, cluster, cache};

@@ -2,8 +2,9 @@
 
 Covers the hand-worked examples, random tie-heavy rows (signed zeros, infinities, NaN,
 counts below zero, past the row and between), rows that are not 16-byte aligned, the
-single-CTA path (many rows) and the cluster path (few long rows), all-equal rows, and the
-two full-size workloads of ``synth.topk_config``.
+single-CTA path (many rows), the cluster path (few long rows), rows longer than the
+shared-memory key cache, all-equal rows (candidate lists overflow), and the two full-size
+workloads of ``synth.topk_config``.
 """
 import numpy as np
 import pytest
@@ -87,6 +88,18 @@ def test_topk_cluster_rows(T, width, K):
     sc = synth.indexer_scores(rng, T, width)
     nc = rng.integers(width // 2, width + 1, size=T).astype(np.int32)
     assert_same(sc, nc, K, what=f"T={T} width={width} K={K}")
+
+
+def test_topk_uncached_rows():
+    """Many long rows: one CTA a row whose 45000 candidates exceed the shared-memory key cache, so
+    every pass reads the scores from global memory."""
+    need_gpu()
+    rng = np.random.default_rng(91)
+    T, width, K = 96, 45000, 2048
+    sc = synth.indexer_scores(rng, T, width)
+    nc = rng.integers(40000, width + 1, size=T).astype(np.int32)
+    nc[0] = width
+    assert_same(sc, nc, K, what="uncached rows")
 
 
 def test_topk_extreme_ties():
