@@ -639,7 +639,10 @@ def run_combine_compressed(args):
                                    "region, window 128, rows of 2304", "tokens_per_step": T, "replicas": reps,
                        "l2": f"inputs larger than L2: {reps} rotating replicas"},
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                         "traffic": None, "kernel": "combine_compressed_kernel",
+                         "traffic": traffic_record("combine_compressed_kernel",
+                                                   "compressed combine: 64 requests x 4 tokens, top-k 2048 of a "
+                                                   "4x-compressed region, window 128, rows of 2304"),
+                         "kernel": "combine_compressed_kernel",
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
                          "algorithmic_bytes_per_launch": bytes_per_step,
                          "timed": "one call (one launch) per step, CUDA events on the launching stream"},
@@ -721,7 +724,7 @@ def run_topk_select(args):
             "config": {"workload": desc, "tokens_per_step": T, "candidates_per_step": int(nc.sum()), "top_k": K,
                        "replicas": reps, "l2": f"inputs larger than L2: {reps} rotating replicas"},
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                         "traffic": None, "kernel": "topk_select_kernel",
+                         "traffic": traffic_record("topk_select_kernel", desc), "kernel": "topk_select_kernel",
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
                          "algorithmic_bytes_per_launch": bytes_per_step,
                          "timed": "one call (one launch) per step, CUDA events on the launching stream"},
@@ -810,7 +813,10 @@ def run_qnorm_rope_insert(args):
                        "tokens_per_step": T, "heads": H, "replicas": reps,
                        "l2": f"inputs larger than L2: {reps} rotating replicas"},
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                         "traffic": None, "kernel": "qnorm_rope_kv_insert_kernel",
+                         "traffic": traffic_record("qnorm_rope_kv_insert_kernel",
+                                                   "q RMSNorm + GPT-J RoPE + FP8 KV insert: 128 tokens x 128 heads, "
+                                                   "65536-slot cache"),
+                         "kernel": "qnorm_rope_kv_insert_kernel",
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
                          "algorithmic_bytes_per_launch": bytes_per_step,
                          "timed": "one call (one launch) per step, CUDA events on the launching stream"},
