@@ -194,6 +194,24 @@ def cpu_baseline(w, seconds: float):
                       f"({el:.1f} s, fp64, one thread per token)"}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's value: the whole job's time is its slowest rank's (one rank:
+    the value itself)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes its own units_per_rank,
+    all of them within the slowest rank's ms."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -388,12 +406,8 @@ def run_ours(args):
         time.sleep(0.2)
         sampler.stop()
     clocks = sampler.summary(h0, h1) if rank == 0 else None
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-
-    value = world * T * args.steps / (ms / 1e3)
+    ms = max_over_ranks(ms, dev)
+    value = job_rate(T * args.steps, world, ms)
 
     # roofline of the decode call, timed with CUDA events over the timed region (64/128 heads: one
     # kernel that combines, decodes and merges; 16/32 heads: combine, decode and merge kernels)
@@ -523,11 +537,8 @@ def run_ours(args):
         last = ((e_rem if e_rem else G) - 1) & 1
         if not torch.equal(h_res[last][:out_bytes].view(torch.int16), outs[0].view(torch.int16).reshape(-1).cpu()):
             raise RuntimeError("end-to-end output differs from the device-timed output")
-        if world > 1:
-            t = torch.tensor([ems], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * T * n_e2e / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        ems = max_over_ranks(ems, dev)
+        e2e = {"value": job_rate(T * n_e2e, world, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "method": "per step: one pinned H2D copy of q/topk/seq_lens/block_table (packed), the C-ABI call, "
                          "one D2H copy of out+lse; copies on their own streams, double-buffered, overlapping "
