@@ -154,6 +154,18 @@ DSV4_API dsv4_status dsv4_combine_topk_swa_indices_compressed(
     int64_t combined_stride, int32_t combined_width, int32_t *combined_lens, dsv4_stream_t stream);
 
 /*
+ * dsv4_selftest_wait_timeout -- checks the bounded waits and the status path without a fault.
+ *
+ * Every wait of the tensor-core decode kernel on an mbarrier gives up after a limit (about two
+ * seconds), records DSV4_ERR_TIMEOUT in the device status word and lets the kernel run to its
+ * end, so a lost arrival never hangs the GPU.  This call launches one small kernel whose single
+ * thread runs that same bounded wait, with a limit of `cycles` SM clock cycles (1 .. 2^31), on
+ * an mbarrier nothing arrives on: the next dsv4_get_device_status returns DSV4_ERR_TIMEOUT and
+ * the context stays usable.  Returns DSV4_OK, DSV4_ERR_INVALID_ARG or DSV4_ERR_CUDA.
+ */
+DSV4_API dsv4_status dsv4_selftest_wait_timeout(int64_t cycles, dsv4_stream_t stream);
+
+/*
  * dsv4_qnorm_rope_kv_insert -- the step before the decode: normalise and rotate the queries and
  * write each token's key into the FP8 cache.
  *

@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "DSV4_OK", 1: "DSV4_ERR_INVALID_ARG", 2: "DSV4_ERR_BAD_INDEX"
                 4: "DSV4_ERR_CUDA", 5: "DSV4_ERR_UNSUPPORTED"}
 
 EXPORTED = ("dsv4_combine_topk_swa_indices", "dsv4_combine_topk_swa_indices_compressed", "dsv4_topk_select",
-            "dsv4_qnorm_rope_kv_insert",
+            "dsv4_qnorm_rope_kv_insert", "dsv4_selftest_wait_timeout",
             "dsv4_sparse_mla_decode_workspace_size", "dsv4_sparse_mla_decode", "dsv4_sparse_mla_decode_noalloc",
             "dsv4_get_device_status")
 
@@ -68,6 +68,8 @@ def load_library():
     lib.dsv4_combine_topk_swa_indices_compressed.restype = ctypes.c_int
     lib.dsv4_combine_topk_swa_indices_compressed.argtypes = [P, i64, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                              P, i64, i32, P, P]
+    lib.dsv4_selftest_wait_timeout.restype = ctypes.c_int
+    lib.dsv4_selftest_wait_timeout.argtypes = [i64, P]
     lib.dsv4_qnorm_rope_kv_insert.restype = ctypes.c_int
     lib.dsv4_qnorm_rope_kv_insert.argtypes = [P, i64, P, i64, i32, i32, P, ctypes.c_float, P, i64, P, P, P, i32, P,
                                               i64, P]
@@ -145,6 +147,11 @@ def dsv4_combine_topk_swa_indices_compressed(topk_idx: torch.Tensor, query_start
         _ptr(gather_lens), query_start_loc.numel() - 1, T, int(region_stride), int(compressed_len), int(top_k),
         int(compress_ratio), int(window), _ptr(combined), max(combined.stride(0), combined.shape[1]),
         combined.shape[1], _ptr(combined_lens), _stream(stream))
+
+
+def dsv4_selftest_wait_timeout(cycles: int, stream=None) -> int:
+    """One bounded wait on an mbarrier nothing arrives on (see include/dsv4.h)."""
+    return load_library().dsv4_selftest_wait_timeout(int(cycles), _stream(stream))
 
 
 def dsv4_qnorm_rope_kv_insert(q: torch.Tensor, q_out: torch.Tensor, kv: torch.Tensor, positions: torch.Tensor,

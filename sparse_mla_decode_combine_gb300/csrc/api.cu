@@ -236,6 +236,18 @@ extern "C" DSV4_API dsv4_status dsv4_combine_topk_swa_indices_compressed(
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
+extern "C" DSV4_API dsv4_status dsv4_selftest_wait_timeout(int64_t cycles, dsv4_stream_t stream)
+{
+    if (cycles < 1 || cycles > (int64_t)1 << 31)
+        return DSV4_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    if (device_info(&status, nullptr) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    return launch_wait_selftest((long long)cycles, status, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DSV4_OK
+               : DSV4_ERR_CUDA;
+}
+
 extern "C" DSV4_API dsv4_status dsv4_qnorm_rope_kv_insert(
     const void *q, int64_t q_token_stride, void *q_out, int64_t q_out_token_stride, int32_t num_tokens,
     int32_t num_heads, const float *q_norm_weight, float eps, const void *kv, int64_t kv_token_stride,

@@ -145,13 +145,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 
 // Bounded wait on one phase of an mbarrier by a single thread.  After any timeout in
 // the CTA (abort flag set) waits return at once, so the CTA still reaches its end.
-__device__ __noinline__ void mbar_wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *status)
+__device__ __noinline__ void mbar_wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *status,
+                                           long long limit = kWaitCycles)
 {
     if (*abort_flag)
         return;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             atomicOr(status, kStatusTimeout);
             return;
@@ -1069,7 +1070,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     }
 }
 
+// Self-test of the bounded waits: one thread waits, at most `limit` SM cycles, on an mbarrier
+// that nothing arrives on; the wait gives up, sets the abort flag and the timeout bit, and the
+// kernel ends normally.
+__global__ void wait_selftest_kernel(long long limit, unsigned *status)
+{
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        abort_flag = 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_wait_one(smem_u32(&bar), 0u, &abort_flag, status, limit);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(long long limit, unsigned *status, cudaStream_t stream)
+{
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(limit, status);
+    return cudaGetLastError();
+}
 
 int decode_tc_max_splits() { return kMaxSplits; }
 int decode_tc_block_keys() { return kBK; }

@@ -120,6 +120,7 @@ cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
 int decode_tc_block_keys();
+cudaError_t launch_wait_selftest(long long limit, unsigned *status, cudaStream_t stream);
 int decode_tc_table_bits(int topk_width);   // combine hash set of the tensor-core kernel: 2^bits 8-byte slots
 int decode_tc_max_splits();
 int decode_tc_resident_ctas(int splits);

@@ -73,6 +73,9 @@ def test_host_side_argument_errors(lib):
     assert tk(P, 16, 16, P, 1, 4, P, 3, None, S) == pkg.DSV4_ERR_INVALID_ARG
     assert tk(P, 8, 16, P, 1, 4, P, 4, None, S) == pkg.DSV4_ERR_INVALID_ARG
     assert tk(None, 0, 0, None, 0, 4, None, 0, None, S) == pkg.DSV4_OK
+    # wait self-test: a limit out of range
+    assert lib.dsv4_selftest_wait_timeout(0, S) == pkg.DSV4_ERR_INVALID_ARG
+    assert lib.dsv4_selftest_wait_timeout((1 << 31) + 1, S) == pkg.DSV4_ERR_INVALID_ARG
     # fused norm/RoPE/insert: heads 0 and 129, NaN eps, odd stride, nothing to do
     ins = lib.dsv4_qnorm_rope_kv_insert
     #         q, qs,   qo, qos,  T, H,  w,    eps,  kv, kvs, pos, slot, cs, maxp, cache, nslots, stream
