@@ -24,11 +24,19 @@ def run(topk, qsl, seqs, gls, M, N, top_k, C, W, width, num_tokens=None):
     q = torch.from_numpy(np.asarray(qsl, dtype=np.int32)).to(dev)
     s = torch.from_numpy(np.asarray(seqs, dtype=np.int32)).to(dev)
     g = torch.from_numpy(np.asarray(gls, dtype=np.int32)).to(dev)
-    out = torch.full((T, width), 12345, dtype=torch.int32, device=dev)
-    lens = torch.full((T,), 12345, dtype=torch.int32, device=dev)
+    # guard bands around the outputs (and a row stride wider than the row) catch stray writes
+    out_full = torch.full((T + 2, width + 16), 0x5A5A5A5A, dtype=torch.int32, device=dev)
+    out = out_full[1:T + 1, 8:8 + width]
+    lens_full = torch.full((T + 16,), 0x5A5A5A5A, dtype=torch.int32, device=dev)
+    lens = lens_full[8:8 + T]
     pkg.check(pkg.dsv4_combine_topk_swa_indices_compressed(tk, q, s, g, M, N, top_k, C, W, out, lens),
               "compressed combine")
     torch.cuda.synchronize()
+    of = out_full.cpu().numpy()
+    assert np.all(of[0] == 0x5A5A5A5A) and np.all(of[-1] == 0x5A5A5A5A)
+    assert np.all(of[:, :8] == 0x5A5A5A5A) and np.all(of[:, 8 + width:] == 0x5A5A5A5A)
+    lf = lens_full.cpu().numpy()
+    assert np.all(lf[:8] == 0x5A5A5A5A) and np.all(lf[8 + T:] == 0x5A5A5A5A)
     return out.cpu().numpy(), lens.cpu().numpy()
 
 

@@ -27,10 +27,18 @@ def run_gpu(scores: np.ndarray, num_cand, top_k: int, stride: int = 0):
     buf[:, :width] = torch.from_numpy(scores)
     sc = buf.cuda()[:, :width]
     nc = torch.from_numpy(np.asarray(num_cand, dtype=np.int32)).cuda()
-    idx = torch.full((T, top_k), -7, dtype=torch.int32, device="cuda")
-    lens = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    # guard bands around the outputs (and a row stride wider than the row) catch stray writes
+    idx_full = torch.full((T + 2, top_k + 16), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    idx = idx_full[1:T + 1, 8:8 + top_k]
+    lens_full = torch.full((T + 16,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    lens = lens_full[8:8 + T]
     pkg.check(pkg.dsv4_topk_select(sc, nc, top_k, idx, lens), "topk_select")
     torch.cuda.synchronize()
+    xf = idx_full.cpu().numpy()
+    assert np.all(xf[0] == 0x5A5A5A5A) and np.all(xf[-1] == 0x5A5A5A5A)
+    assert np.all(xf[:, :8] == 0x5A5A5A5A) and np.all(xf[:, 8 + top_k:] == 0x5A5A5A5A)
+    lf = lens_full.cpu().numpy()
+    assert np.all(lf[:8] == 0x5A5A5A5A) and np.all(lf[8 + T:] == 0x5A5A5A5A)
     return idx.cpu().numpy(), lens.cpu().numpy()
 
 
