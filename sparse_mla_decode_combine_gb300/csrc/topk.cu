@@ -344,59 +344,46 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     // ---- the keys in round 0's bin become candidates (key, position), each warp listing those
     // of its chunk in position order; keys above the bin are selected whatever the later rounds
     // find: they are counted, and (with the cache) marked in the bitmap
-    uint32_t sure = 0u, nw = 0u;   // per lane: keys above the bin; per warp: candidates so far
+    uint32_t sure = 0u, nw = 0u;   // per warp (the same in every lane): keys above the bin, candidates so far
     uint32_t *wkey = ckey + warp * kTkCandWarp;
     uint32_t *wpos = cpos + warp * kTkCandWarp;
-    for (int i0 = c_lo; i0 < c_hi; i0 += 128) {   // four consecutive keys a lane, 8 lanes a bitmap word
-        const int i = i0 + 4 * lane;
+    const uint32_t below = (1u << lane) - 1u;
+    for (int i0 = c_lo; i0 < c_hi; i0 += 128) {   // lane l takes positions i0 + 32 j + l: a bitmap word is a ballot
+        const bool full = cache && i0 + 128 <= c_hi;
         uint32_t k[4];
-        if (cache && i + 4 <= c_hi) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(kc + i);
-            k[0] = v.x;
-            k[1] = v.y;
-            k[2] = v.z;
-            k[3] = v.w;
-        } else {
+        if (full) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                k[j] = i + j < c_hi ? key_at(i + j) : 0u;
+                k[j] = kc[i0 + 32 * j + lane];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + 32 * j + lane;
+                k[j] = i < c_hi ? key_at(i) : 0u;
+            }
         }
-        uint32_t bits = 0u, nc = 0u;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const bool in = i + j < c_hi;
-            const bool up = in && (k[j] >> 21) > d0;
-            sure += up ? 1u : 0u;
-            bits |= up ? 1u << (4 * (lane & 7) + j) : 0u;
-            nc += (in && (k[j] >> 21) == d0) ? 1u : 0u;
-        }
-        uint32_t incl = nc;   // candidates up to this lane's four keys, in position order
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o)
-                incl += y;
-        }
-        uint32_t slot = nw + incl - nc;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (i + j < c_hi && (k[j] >> 21) == d0) {
-                if (slot < (uint32_t)kTkCandWarp) {
-                    wkey[slot] = k[j];
-                    wpos[slot] = (uint32_t)(i + j);
+            const int i = i0 + 32 * j + lane;
+            const bool in = full || i < c_hi;
+            const uint32_t dg = k[j] >> 21;
+            const uint32_t bu = __ballot_sync(0xffffffffu, in && dg > d0);
+            const uint32_t bc = __ballot_sync(0xffffffffu, in && dg == d0);
+            sure += (uint32_t)__popc(bu);
+            if (bc != 0u) {   // candidates in position order: (j, lane) is position order within the 128
+                if ((bc >> lane) & 1u) {
+                    const uint32_t slot = nw + (uint32_t)__popc(bc & below);
+                    if (slot < (uint32_t)kTkCandWarp) {
+                        wkey[slot] = k[j];
+                        wpos[slot] = (uint32_t)i;
+                    }
                 }
-                ++slot;
+                nw += (uint32_t)__popc(bc);
             }
-        nw += __shfl_sync(0xffffffffu, incl, 31);
-        bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
-        bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
-        bits |= __shfl_xor_sync(0xffffffffu, bits, 4);
-        if (cache && (lane & 7) == 0 && i < c_hi)
-            bm[i >> 5] = bits;
+            if (cache && lane == j && i0 + 32 * j < c_hi)
+                bm[(i0 >> 5) + j] = bu;
+        }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        sure += __shfl_xor_sync(0xffffffffu, sure, o);
     if (lane == 0) {
         wsure[warp] = sure;
         wncand[warp] = nw;
@@ -433,48 +420,52 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     const uint32_t vstar = prefix;   // the K-th largest key; rem keys equal to it are taken
 
     // ---- (> v*, == v*) per warp chunk, then per segment and the segments' offsets
-    if (tid < kTkWarps) {
-        wcnt[tid][0] = listed ? wsure[tid] : 0u;
-        wcnt[tid][1] = 0u;
-    }
-    __syncthreads();
-    if (listed) {
-        for (int c = tid; c < kTkCandMax; c += kTkThreads) {
-            const int w = c / kTkCandWarp;
-            if ((uint32_t)(c % kTkCandWarp) < wncand[w]) {
-                const uint32_t k = ckey[c];
-                if (k > vstar)
-                    atomicAdd(&wcnt[w][0], 1u);
-                else if (k == vstar)
-                    atomicAdd(&wcnt[w][1], 1u);
+    {
+        uint32_t ng = 0u, ne = 0u;
+        if (listed) {   // the warp's own list, plus the keys above round 0's bin
+            const uint32_t nwc = wncand[warp];
+            for (uint32_t c = lane; c < nwc; c += 32) {
+                const uint32_t k = wkey[c];
+                ng += k > vstar ? 1u : 0u;
+                ne += k == vstar ? 1u : 0u;
+            }
+        } else {
+            for (int i = c_lo + lane; i < c_hi; i += 32) {
+                const uint32_t k = key_at(i);
+                ng += k > vstar ? 1u : 0u;
+                ne += k == vstar ? 1u : 0u;
             }
         }
-    } else {
-        uint32_t ng = 0u, ne = 0u;
-        for (int i = c_lo + lane; i < c_hi; i += 32) {
-            const uint32_t k = key_at(i);
-            ng += k > vstar;
-            ne += k == vstar;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            ng += __shfl_xor_sync(0xffffffffu, ng, o);
-            ne += __shfl_xor_sync(0xffffffffu, ne, o);
-        }
+        ng = __reduce_add_sync(0xffffffffu, ng);
+        ne = __reduce_add_sync(0xffffffffu, ne);
         if (lane == 0) {
-            wcnt[warp][0] = ng;
+            wcnt[warp][0] = ng + (listed ? wsure[warp] : 0u);
             wcnt[warp][1] = ne;
         }
     }
     __syncthreads();
-    uint32_t gt_local = 0u, eq_local = 0u, wg = 0u, we = 0u;
-    for (int w = 0; w < kTkWarps; ++w) {
-        if (w == warp) {
-            wg = gt_local;
-            we = eq_local;
+    // every warp scans the chunk counts: lane w holds chunk w's
+    uint32_t gt_local, eq_local, wg, we;
+    {
+        uint32_t g = lane < kTkWarps ? wcnt[lane][0] : 0u;
+        uint32_t e = lane < kTkWarps ? wcnt[lane][1] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t yg = __shfl_up_sync(0xffffffffu, g, o);
+            const uint32_t ye = __shfl_up_sync(0xffffffffu, e, o);
+            if (lane >= o) {
+                g += yg;
+                e += ye;
+            }
         }
-        gt_local += wcnt[w][0];
-        eq_local += wcnt[w][1];
+        gt_local = __shfl_sync(0xffffffffu, g, 31);
+        eq_local = __shfl_sync(0xffffffffu, e, 31);
+        wg = __shfl_sync(0xffffffffu, g, (warp + 31) & 31);   // inclusive sum of chunks before this warp's
+        we = __shfl_sync(0xffffffffu, e, (warp + 31) & 31);
+        if (warp == 0) {
+            wg = 0u;
+            we = 0u;
+        }
     }
     if (tid < CL) {
         put(&cnt[rank][0], tid, gt_local);
