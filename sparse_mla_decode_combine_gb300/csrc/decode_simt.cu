@@ -13,8 +13,11 @@
 //      (running max / running sum per head) and accumulates P.V in registers.
 // At the end it either normalises (one split: sink folded into the normaliser,
 // BF16 out, natural-log LSE) or stores the unnormalised partial for the merge.
-// At 16-32 heads the logits are a thin product (<= 32 x 576 per key) that the
-// CUDA cores keep up with; the kernel is bound by the gather.
+// The cache slots of tile i + 2 are resolved, and the raw entries of tile i + 1 loaded into
+// registers, while tile i is computed; the softmax runs on all threads (the threads of a head
+// are one group of lanes and keep its running max and sum in registers).  Each key costs
+// 2 * 16..32 * 1088 fp32 FLOPs against 656 bytes: on CUDA cores the kernel is bound by the
+// FMA rate, not by the gather.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -70,21 +73,40 @@ __device__ __forceinline__ void e4m3x16_to_f32(const uint4 v, float scale, float
     }
 }
 
+// Cache slot of logical position idx of block-table row `row` (-1, and the bad-index bit in the
+// status word, when the position or its page is outside the table or the cache).
+__device__ __forceinline__ int slot_of(const DecodeParams &p, int row, int idx, int phys)
+{
+    if (idx < 0 || phys < 0 || phys >= p.num_blocks) {
+        atomicOr(p.status, kStatusBadIndex);
+        return -1;
+    }
+    return phys * p.page + (idx - (idx / p.page) * p.page);
+}
+
+__device__ __forceinline__ int page_of(const DecodeParams &p, int row, int idx)
+{
+    const int blk = idx >= 0 ? idx / p.page : -1;
+    return (idx >= 0 && blk < p.max_blocks) ? __ldg(p.block_table + (int64_t)row * p.bt_stride + blk) : -1;
+}
+
 template <int HG>
 __global__ void __launch_bounds__(kThreads, 1) decode_simt_kernel(const DecodeParams p)
 {
     static_assert(HG == 16 || HG == 32, "head group");
-    constexpr int TPH = kThreads / HG;          // threads per head in the P.V stage
+    constexpr int TPH = kThreads / HG;          // threads per head in the softmax and P.V stages
     constexpr int NV4 = kLatent / (4 * TPH);    // float4 accumulators per thread
     constexpr int KPL = HG / 8;                 // keys per lane in the logit stage
+    constexpr int KPT = kTile / TPH;            // keys per thread in the softmax
+    constexpr int kPieces = 40;                 // 16-byte data pieces of an entry (32 latent, 8 rope)
+    constexpr int kLoads = kTile * kPieces / kThreads;
+    static_assert(kTile * kPieces % kThreads == 0, "gather pieces per thread");
 
     extern __shared__ __align__(16) float smem[];
     float *qs = smem;                 // [HG][kRow]
     float *ks = qs + HG * kRow;       // [kTile][kRow]
     float *ss = ks + kTile * kRow;    // [HG][kScoreRow]
-    __shared__ long long rowoff[kTile];
-    __shared__ float rscale[kTile][4];
-    __shared__ float s_alpha[HG], s_m[HG], s_l[HG];
+    __shared__ int ring[3][kTile];    // cache slots of tiles i, i+1, i+2 (slot -1: no key)
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -99,11 +121,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_simt_kernel(const DecodePa
     const int L = p.lens[t];
     const int kbeg = split * p.chunk;
     const int kend = min(L, kbeg + p.chunk);
+    const int ntiles = kend > kbeg ? (kend - kbeg + kTile - 1) / kTile : 0;
     const int row = p.req_idx ? p.req_idx[t] : t;
     const bool row_ok = row >= 0 && row < p.num_reqs;
     if (!row_ok && tid == 0 && kend > kbeg)
         atomicOr(p.status, kStatusBadIndex);
+    const int32_t *crow = p.combined + (int64_t)t * p.cw;
 
+    // slots of tiles 0 and 1 (one round trip through the combined list and the block table)
+    if (tid < 2 * kTile) {
+        const int k = kbeg + tid;
+        int sl = -1;
+        if (row_ok && k < kend) {
+            const int idx = crow[k];
+            sl = slot_of(p, row, idx, page_of(p, row, idx));
+        }
+        ring[tid / kTile][tid % kTile] = sl;
+    }
     // Q (BF16) -> fp32 rows
     for (int i = tid; i < HG * (kDim / 8); i += kThreads) {
         const int h = i / (kDim / 8);
@@ -111,63 +145,64 @@ __global__ void __launch_bounds__(kThreads, 1) decode_simt_kernel(const DecodePa
         const uint4 v = *reinterpret_cast<const uint4 *>(p.q + (int64_t)t * p.q_token_stride + (int64_t)(h0 + h) * kDim + 8 * c);
         bf16x8_to_f32(v, qs + h * kRow + 8 * c);
     }
-    if (tid < HG) {
-        s_m[tid] = -INFINITY;
-        s_l[tid] = 0.f;
-    }
-    const int ph = tid / TPH;   // head of this thread in the P.V stage
+    const int ph = tid / TPH;   // head of this thread in the softmax and P.V stages
     const int pg = tid % TPH;
+    float m_run = -INFINITY, l_run = 0.f;   // the head's running max and row sum (same in its TPH threads)
     float4 acc[NV4];
 #pragma unroll
     for (int i = 0; i < NV4; ++i)
         acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
 
-    for (int k0 = kbeg; k0 < kend; k0 += kTile) {
-        const int nk = min(kTile, kend - k0);
-        // 1. logical position -> cache byte offset, and the row's four scales
-        if (tid < kTile) {
-            long long off = -1;
-            if (tid < nk && row_ok) {
-                const int idx = p.combined[(int64_t)t * p.cw + k0 + tid];
-                const int blk = idx >= 0 ? idx / p.page : -1;
-                int phys = -1;
-                if (idx >= 0 && blk < p.max_blocks)
-                    phys = p.block_table[(int64_t)row * p.bt_stride + blk];
-                if (phys >= 0 && phys < p.num_blocks)
-                    off = ((long long)phys * p.page + (idx - blk * p.page)) * kEntryBytes;
-                else
-                    atomicOr(p.status, kStatusBadIndex);
-            }
-            rowoff[tid] = off;
-            unsigned sw = 0;
-            if (off >= 0)
-                sw = __ldg(reinterpret_cast<const unsigned *>(p.kv + off + kScaleOffset));
+    // the raw pieces of the next tile, in registers: piece c = tid + kThreads u is piece c % 40 of row c / 40
+    uint4 raw[kLoads];
+    unsigned rsc[kLoads];
+    auto load_tile = [&](const int *sl) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-                rscale[tid][b] = ue8m0_to_float((sw >> (8 * b)) & 0xFFu);
-        }
-        __syncthreads();
-        // 2. gather + dequantise: 40 data chunks of 16 bytes per row (32 latent, 8 rope)
-        for (int c = tid; c < kTile * 40; c += kThreads) {
-            const int r = c / 40;
-            const int j = c % 40;
-            const long long off = rowoff[r];
-            float *dst = ks + r * kRow + (j < 32 ? 16 * j : kLatent + 8 * (j - 32));
-            const int nv = j < 32 ? 16 : 8;
-            if (off < 0) {
-                for (int e = 0; e < nv; e += 4)
-                    *reinterpret_cast<float4 *>(dst + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-                continue;
+        for (int u = 0; u < kLoads; ++u) {
+            const int c = tid + kThreads * u;
+            const int s = sl[c / kPieces];
+            const int j = c % kPieces;
+            raw[u] = make_uint4(0u, 0u, 0u, 0u);
+            rsc[u] = 0u;
+            if (s >= 0) {
+                const uint8_t *e = p.kv + (int64_t)s * kEntryBytes;
+                raw[u] = __ldg(reinterpret_cast<const uint4 *>(e + 16 * j));
+                if (j < 32)
+                    rsc[u] = __ldg(reinterpret_cast<const unsigned *>(e + kScaleOffset));
             }
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.kv + off + 16 * j));
-            if (j < 32)
-                e4m3x16_to_f32(v, rscale[r][j >> 3], dst);
-            else
-                bf16x8_to_f32(v, dst);
         }
+    };
+    if (ntiles > 0)
+        load_tile(ring[0]);
+
+    for (int it = 0; it < ntiles; ++it) {
+        const int k0 = kbeg + it * kTile;
+        const int nk = min(kTile, kend - k0);
+        const int *sl = ring[it % 3];
+        // tile it + 2: its positions now, its pages after the dequant, its slots after the logits
+        int idx2 = -1, pg2 = -1;
+        const bool has2 = warp == 0 && row_ok && k0 + 2 * kTile + lane < kend;
+        if (has2)
+            idx2 = crow[k0 + 2 * kTile + lane];
+        // 1. dequantise the registers into the key tile (rows without a key are zeros)
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) {
+            const int c = tid + kThreads * u;
+            const int r = c / kPieces;
+            const int j = c % kPieces;
+            float *dst = ks + r * kRow + (j < 32 ? 16 * j : kLatent + 8 * (j - 32));
+            if (j < 32)
+                e4m3x16_to_f32(raw[u], ue8m0_to_float((rsc[u] >> (8 * (j >> 3))) & 0xFFu), dst);
+            else
+                bf16x8_to_f32(raw[u], dst);
+        }
+        if (has2)
+            pg2 = page_of(p, row, idx2);
         __syncthreads();
-        // 3. logits: lane -> head, each lane KPL keys of this warp's four
+        if (it + 1 < ntiles)
+            load_tile(ring[(it + 1) % 3]);
+        // 2. logits: lane -> head, each lane KPL keys of this warp's four
         {
             const int h = lane % HG;
             const int kb = 4 * warp + (lane / HG) * KPL;
@@ -191,45 +226,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_simt_kernel(const DecodePa
 #pragma unroll
             for (int k = 0; k < KPL; ++k) {
                 const int j = kb + k;
-                ss[h * kScoreRow + j] = (j < nk && rowoff[j] >= 0) ? a[k] * p.scale : -INFINITY;
+                ss[h * kScoreRow + j] = (j < nk && sl[j] >= 0) ? a[k] * p.scale : -INFINITY;
             }
         }
+        if (warp == 0 && k0 + 2 * kTile < kend)   // ring slot of tile it - 1, done with
+            ring[(it + 2) % 3][lane] = has2 ? slot_of(p, row, idx2, pg2) : -1;
         __syncthreads();
-        // 4. online softmax update, one thread per head
-        if (tid < HG) {
-            float *sr = ss + tid * kScoreRow;
-            const float mo = s_m[tid];
+        // 3. online softmax: the TPH threads of head ph (one warp) take KPT keys each
+        {
+            float *sr = ss + ph * kScoreRow + pg * KPT;
+            float sv[KPT];
             float mt = -INFINITY;
-            for (int j = 0; j < kTile; ++j)
-                mt = fmaxf(mt, sr[j]);
-            const float mn = fmaxf(mo, mt);
-            float alpha = 1.f;
-            float sum = 0.f;
-            if (mn == -INFINITY) {
-                for (int j = 0; j < kTile; ++j)
-                    sr[j] = 0.f;
-            } else {
-                alpha = expf(mo - mn);
-                for (int j = 0; j < kTile; ++j) {
-                    const float e = expf(sr[j] - mn);
-                    sr[j] = e;
+#pragma unroll
+            for (int u = 0; u < KPT; ++u) {
+                sv[u] = sr[u];
+                mt = fmaxf(mt, sv[u]);
+            }
+#pragma unroll
+            for (int o = TPH / 2; o > 0; o >>= 1)
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+            const float mn = fmaxf(m_run, mt);
+            float alpha = 1.f, sum = 0.f;
+            if (mn != -INFINITY) {
+                alpha = expf(m_run - mn);
+#pragma unroll
+                for (int u = 0; u < KPT; ++u) {
+                    const float e = expf(sv[u] - mn);
+                    sr[u] = e;
                     sum += e;
                 }
+            } else {
+#pragma unroll
+                for (int u = 0; u < KPT; ++u)
+                    sr[u] = 0.f;
             }
-            s_l[tid] = s_l[tid] * alpha + sum;
-            s_m[tid] = mn;
-            s_alpha[tid] = alpha;
-        }
-        __syncthreads();
-        // 5. O = alpha * O + P.V
-        {
-            const float al = s_alpha[ph];
+#pragma unroll
+            for (int o = TPH / 2; o > 0; o >>= 1)
+                sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            l_run = l_run * alpha + sum;
+            m_run = mn;
+            __syncwarp();
+            // 4. O = alpha * O + P.V
 #pragma unroll
             for (int i = 0; i < NV4; ++i) {
-                acc[i].x *= al;
-                acc[i].y *= al;
-                acc[i].z *= al;
-                acc[i].w *= al;
+                acc[i].x *= alpha;
+                acc[i].y *= alpha;
+                acc[i].z *= alpha;
+                acc[i].w *= alpha;
             }
             const float *pr = ss + ph * kScoreRow;
             for (int j = 0; j < nk; ++j) {
@@ -249,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_simt_kernel(const DecodePa
     }
 
     const int h = h0 + ph;
-    const float m = s_m[ph];
-    const float l = s_l[ph];
+    const float m = m_run;
+    const float l = l_run;
     if (p.splits == 1) {
         float mf = m;
         float lf = l;
