@@ -411,7 +411,7 @@ def run_ours(args):
 
     # roofline of the decode call, timed with CUDA events over the timed region (64/128 heads: one
     # kernel that combines, decodes and merges; 16/32 heads: combine, decode and merge kernels)
-    launches_per_step = 1 if H >= 64 else 3
+    launches_per_step = 1
     hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
     call_s = ms / 1e3 / args.steps
     t_hbm = bytes_per_step / (hbm_peak * 1e9)
@@ -423,13 +423,13 @@ def run_ours(args):
         ach = flops_per_step / call_s / 1e12
         roofline = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s",
                     "frac": ach / bf16_peak}
-    decode_kernel = "decode_tc_kernel" if H >= 64 else "decode_simt_kernel"
+    decode_kernel = "decode_tc_kernel"
     roofline.update({
         "traffic": traffic_record(decode_kernel, w.name),
         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
         "kernel": decode_kernel,
-        "timed": ("whole decode call per step (64/128 heads: the one kernel that combines, decodes and merges "
-                  "its splits; 16/32 heads: combine, decode and merge kernels), CUDA events on the launching "
+        "timed": ("whole decode call per step (one kernel that combines, decodes and merges its splits), "
+                  "CUDA events on the launching "
                   "stream over the timed region; per-kernel shares of the step are in ncu_shares (committed ncu "
                   "launch list)"),
         "call_us": call_s * 1e6,

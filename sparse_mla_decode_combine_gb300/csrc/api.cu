@@ -53,7 +53,6 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 constexpr int kMaxWindow = 1 << 24;
-constexpr int kSimtTile = 32;
 
 bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sms, Plan *pl)
 {
@@ -62,23 +61,20 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
     if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128)
         return false;
     Plan p{};
-    // 64 / 128 heads: tensor-core kernel, 64 heads per CTA, 128-key blocks, one CTA per SM.
-    // 16 / 32 heads: CUDA-core kernel, all heads in one CTA, 32-key tiles.
-    const bool tc = num_heads >= 64;
-    p.path = tc ? kPathTc : kPathSimt;
-    p.heads_per_group = tc ? 64 : num_heads;
-    p.groups = num_heads / p.heads_per_group;
+    // One tensor-core kernel, 64 heads per CTA (a group of 16 or 32 heads runs as a 64-head group
+    // whose missing heads have zero queries and are never written), 128-key blocks, one CTA per SM.
+    p.heads_per_group = 64;
+    p.groups = (num_heads + p.heads_per_group - 1) / p.heads_per_group;
     p.cw = topk_width + window;
-    const int tile = tc ? decode_tc_block_keys() : kSimtTile;
+    const int tile = decode_tc_block_keys();
     const long long units0 = (long long)(num_tokens > 0 ? num_tokens : 1) * p.groups;
-    // tensor-core path: the splits of a token form one thread-block cluster (<= 8 CTAs)
-    const int split_cap = tc ? decode_tc_max_splits() : merge_max_splits();
+    // the splits of a token form one thread-block cluster (<= 8 CTAs)
+    const int split_cap = decode_tc_max_splits();
     const int max_splits = std::max(1, std::min(split_cap, (p.cw + tile - 1) / tile));
-    // Choose the split count minimising (waves x time per worker).  CUDA-core path: time in
-    // tiles, plus one tile for the global merge when split.  Tensor-core path: a 128-key block
-    // costs its matrix products and softmax whatever its fill, the gather scales with the keys
-    // (chunks are multiples of 16 keys), plus the prologue and, when split, the cluster merge.
-    const int gran = tc ? 16 : tile;
+    // Choose the split count minimising (waves x time per worker): a 128-key block costs its
+    // matrix products and softmax whatever its fill, the gather scales with the keys (chunks are
+    // multiples of 16 keys), plus the prologue and, when split, the cluster merge.
+    const int gran = 16;
     double best = 1e300;
     int best_chunk = std::max(gran, (p.cw + gran - 1) / gran * gran);
     for (int s = 1; s <= max_splits; ++s) {
@@ -88,17 +84,12 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
         if (s_eff > split_cap)
             continue;
         const long long units = units0 * s_eff;
-        const int resident = tc ? decode_tc_resident_ctas(s_eff) : sms;
+        const int resident = decode_tc_resident_ctas(s_eff);
         if (resident <= 0)
             continue;
         const long long waves = (units + resident - 1) / resident;
-        double per_worker;
-        if (tc) {
-            const int blocks = (chunk + tile - 1) / tile;
-            per_worker = blocks + 0.25 * chunk / tile + 0.5 + (s_eff > 1 ? 0.5 : 0.0);
-        } else {
-            per_worker = (double)chunk / tile + (s_eff > 1 ? 1.0 : 0.0);
-        }
+        const int blocks = (chunk + tile - 1) / tile;
+        const double per_worker = blocks + 0.25 * chunk / tile + 0.5 + (s_eff > 1 ? 0.5 : 0.0);
         const double cost = (double)waves * per_worker;
         if (cost < best - 1e-9) {
             best = cost;
@@ -107,20 +98,11 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
     }
     p.chunk = best_chunk;
     p.splits = std::max(1, (p.cw + p.chunk - 1) / p.chunk);
-    p.combine_table_bits = tc ? decode_tc_table_bits(topk_width) : combine_table_bits(topk_width);
+    p.combine_table_bits = decode_tc_table_bits(topk_width);
 
     size_t off = 0;
     p.off_combined = off;
     off = align_up(off + sizeof(int32_t) * (size_t)num_tokens * (size_t)p.cw, 256);
-    p.off_lens = off;
-    off = align_up(off + sizeof(int32_t) * (size_t)num_tokens, 256);
-    p.off_part_o = off;
-    p.off_part_ml = off;
-    if (p.splits > 1 && !tc) {   // the tensor-core kernel merges its splits in shared memory
-        off = align_up(off + sizeof(float) * (size_t)num_tokens * p.splits * num_heads * kLatent, 256);
-        p.off_part_ml = off;
-        off = align_up(off + sizeof(float) * 2 * (size_t)num_tokens * p.splits * num_heads, 256);
-    }
     p.total = std::max<size_t>(off, 256);
     *pl = p;
     return true;
@@ -145,23 +127,6 @@ dsv4_status check_combine_args(const int32_t *topk_idx, int64_t topk_stride, int
 int g_attr_bytes[kMaxDevices][kAttrSlots];
 
 }  // namespace
-
-cudaError_t launch_after_previous(const void *kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
-                                  const DecodeParams &p)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    void *args[] = {const_cast<DecodeParams *>(&p)};
-    return cudaLaunchKernelExC(&cfg, kernel, args);
-}
 
 cudaError_t set_smem_once(const void *kernel, int bytes, AttrSlot slot)
 {
@@ -364,15 +329,12 @@ extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_
     p.req_idx = req_idx;
     p.combined = reinterpret_cast<int32_t *>(ws + pl.off_combined);
     p.cw = pl.cw;
-    p.lens = reinterpret_cast<int32_t *>(ws + pl.off_lens);
     p.num_tokens = num_tokens;
     p.num_heads = num_heads;
     p.sink = sink;
     p.scale = softmax_scale;
     p.out = static_cast<uint16_t *>(out);
     p.lse = lse;
-    p.part_o = reinterpret_cast<float *>(ws + pl.off_part_o);
-    p.part_ml = reinterpret_cast<float *>(ws + pl.off_part_ml);
     p.groups = pl.groups;
     p.heads_per_group = pl.heads_per_group;
     p.splits = pl.splits;
@@ -386,19 +348,8 @@ extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_
     p.window = window;
     p.table_bits = pl.combine_table_bits;
 
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (pl.path == kPathTc) {   // one launch: the kernel combines, decodes and merges its splits
-        e = launch_decode_tc(p, s);
-    } else {
-        e = launch_combine(topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens, window,
-                           reinterpret_cast<int32_t *>(ws + pl.off_combined), pl.cw, pl.cw,
-                           reinterpret_cast<int32_t *>(ws + pl.off_lens), pl.combine_table_bits, s);
-        if (e == cudaSuccess)
-            e = launch_decode_simt(p, s);
-        if (e == cudaSuccess)
-            e = launch_merge(p, s);
-    }
+    // one launch: the kernel combines, decodes and merges its splits
+    const cudaError_t e = launch_decode_tc(p, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 

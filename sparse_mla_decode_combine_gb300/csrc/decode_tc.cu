@@ -21,7 +21,8 @@
 // S^T, O^T (four 128-dv tiles) and per-lane partial row sums live in TMEM (512 columns).
 //
 // CTA = 17 warps, one (token, 64-head group, split): warp 0 issues the MMAs, warps 1-16 do
-// everything else.  Prologue: the CTA combines its token's top-k row with the window
+// everything else.  A token with 16 or 32 heads is one group whose missing heads have zero
+// queries: their columns of the products are computed and dropped, never written out.  Prologue: the CTA combines its token's top-k row with the window
 // (shared-memory hash set for first occurrences, ballot scan for the output order), keeps the
 // entries of its own split and resolves them through the block-table row (cached in shared
 // memory) to cache slots: blocks 0 and 1 straight into shared memory, later blocks into the
@@ -355,7 +356,7 @@ __device__ __noinline__ void cluster_merge_local(uint16_t *out, float *lse, cons
 {
     const int hp = (kNH + S - 1) / S;
     const int hb = rank * hp;
-    const int nh = max(0, min(kNH, hb + hp) - hb);
+    const int nh = max(0, min(min(kNH, num_heads - h0), hb + hp) - hb);   // owned heads that exist
     const int tid = threadIdx.x;
     if (tid < nh) {
         const int h = hb + tid;
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int group = (unit / p.splits) % p.groups;
     const int t = unit / (p.splits * p.groups);
     const int h0 = group * kNH;
+    const int nhv = min(kNH, p.num_heads - h0);   // heads of the group that exist (16 or 32 heads: the rest are zero)
     const bool is_mma = warp == 0;
     const int wid = tid - 32;            // worker index 0..511 (warps 1-16)
 
@@ -573,7 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             const int i = wid + kWorkers * j;
             const int h = i / (kDim / 8);
             const int c = i % (kDim / 8);
-            qv[j] = ld_stream(p.q + (int64_t)t * p.q_token_stride + (int64_t)(h0 + h) * kDim + 8 * c);
+            qv[j] = h < nhv ? ld_stream(p.q + (int64_t)t * p.q_token_stride + (int64_t)(h0 + h) * kDim + 8 * c)
+                            : make_uint4(0u, 0u, 0u, 0u);
         }
     }
 
@@ -693,9 +696,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                          : "memory");
         }
         if (p.splits == 1) {   // zero output, LSE from the sink alone
-            if (tid < kNH && p.lse)
+            if (tid < nhv && p.lse)
                 p.lse[(int64_t)t * p.num_heads + h0 + tid] = p.sink ? p.sink[h0 + tid] : -INFINITY;
-            for (int i = tid; i < kNH * kLatent / 8; i += kThreads) {
+            for (int i = tid; i < nhv * kLatent / 8; i += kThreads) {
                 const int h = i / (kLatent / 8);
                 const int d = i % (kLatent / 8);
                 *reinterpret_cast<uint4 *>(p.out + ((int64_t)t * p.num_heads + h0 + h) * kLatent + 8 * d) =
@@ -994,13 +997,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             if (p.splits == 1) {
                 float M = ms;
                 float Z = lsum;
-                if (p.sink != nullptr) {
+                if (p.sink != nullptr && h < nhv) {
                     const float sk = p.sink[h0 + h];
                     M = fmaxf(ms, sk);
                     Z = (ms == -INFINITY ? 0.f : lsum * expf(ms - M)) + expf(sk - M);
                 }
                 fin[h] = (Z > 0.f && ms != -INFINITY) ? expf(ms - M) / Z : 0.f;
-                if (p.lse)
+                if (p.lse && h < nhv)
                     p.lse[(int64_t)t * p.num_heads + h0 + h] = Z > 0.f ? M + logf(Z) : -INFINITY;
             } else {
                 alpha[h] = ms;
@@ -1022,7 +1025,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int h = hs + j;
-                    p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] = bf16_bits(__uint_as_float(x[j]) * fin[h]);
+                    if (h < nhv)
+                        p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] = bf16_bits(__uint_as_float(x[j]) * fin[h]);
                 }
             }
         }
@@ -1149,7 +1153,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
 {
     if (p.num_tokens <= 0)
         return cudaSuccess;
-    if (p.heads_per_group != kNH || p.chunk <= 0 || p.splits < 1 || p.splits > kMaxSplits || p.topk_width < 0 ||
+    if (p.heads_per_group != kNH || p.num_heads < 1 || p.chunk <= 0 || p.splits < 1 || p.splits > kMaxSplits || p.topk_width < 0 ||
         p.topk_width > kMaxTopkWidth || p.table_bits < 1 || p.table_bits > kHashBitsMax)
         return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(decode_tc_kernel), kSmemBytes, kAttrTc);

@@ -24,20 +24,16 @@ constexpr unsigned kStatusTimeout = 2u;
 
 constexpr int kMaxTopkWidth = 8192;
 
-// Which decode kernel runs a call.
-enum DecodePath { kPathSimt = 0, kPathTc = 1 };
-
 // Work decomposition of one decode call; computed on the host from the call's
 // sizes and the device's SM count, identically by the workspace-size query.
 struct Plan {
-    int path;
-    int heads_per_group;   // heads handled by one worker
-    int groups;            // num_heads / heads_per_group
-    int splits;            // workers sharing one (token, head group); > 1 needs the merge
+    int heads_per_group;   // heads handled by one worker (64: a group of 16 or 32 heads is padded)
+    int groups;            // ceil(num_heads / heads_per_group)
+    int splits;            // workers sharing one (token, head group): one thread-block cluster
     int chunk;             // combined-list entries per split
-    int cw;                // row width of the internal combined list (topk_width + window)
+    int cw;                // row width of the workspace's slot rows (topk_width + window)
     int combine_table_bits;
-    size_t off_combined, off_lens, off_part_o, off_part_ml, total;
+    size_t off_combined, total;
 };
 
 struct DecodeParams {
@@ -51,23 +47,20 @@ struct DecodeParams {
     int32_t max_blocks;
     int32_t num_reqs;
     const int32_t *req_idx;
-    int32_t *combined;         // [T, cw]: combined lists (CUDA-core path) or cache slots (tensor-core path)
+    int32_t *combined;         // [T, cw]: cache slots of the keys past each split's first two blocks
     int32_t cw;
-    const int32_t *lens;       // [T]
     int32_t num_tokens;
     int32_t num_heads;
     const float *sink;
     float scale;
     uint16_t *out;             // BF16 [T, H, 512]
     float *lse;                // [T, H] or null
-    float *part_o;             // CUDA-core path with splits > 1: [T, groups, splits, hpg, 512]
-    float *part_ml;            // CUDA-core path with splits > 1: [T, groups, splits, hpg, 2] (max, sum)
     int32_t groups;
     int32_t heads_per_group;
     int32_t splits;
     int32_t chunk;
     unsigned *status;
-    // the combine's inputs, read by the tensor-core kernel, which combines in its prologue
+    // the combine's inputs: the kernel combines in its prologue
     const int32_t *topk;
     int64_t topk_stride;
     int32_t topk_width;
@@ -80,7 +73,7 @@ struct DecodeParams {
 // Raises a kernel's dynamic shared-memory limit to at least `bytes`, once per
 // (device, kernel slot); later calls with no larger size touch no CUDA state, so a
 // call made after the first one on a device is safe inside stream capture.
-enum AttrSlot { kAttrCombine = 0, kAttrSimt16, kAttrSimt32, kAttrTc, kAttrTopk, kAttrTopkCluster, kAttrSlots };
+enum AttrSlot { kAttrCombine = 0, kAttrTc, kAttrTopk, kAttrTopkCluster, kAttrSlots };
 cudaError_t set_smem_once(const void *kernel, int bytes, AttrSlot slot);
 
 int combine_table_bits(int topk_width);
@@ -97,12 +90,6 @@ cudaError_t launch_combine_compressed(const int32_t *topk, int64_t topk_stride, 
                                       int combined_width, int32_t *combined_lens, unsigned *status,
                                       cudaStream_t stream);
 
-// Launches `kernel(p)` so that it may start while the previous kernel in the stream
-// finishes (programmatic dependent launch); the kernel waits for that kernel's results
-// with griddepcontrol.wait before reading them.
-cudaError_t launch_after_previous(const void *kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
-                                  const DecodeParams &p);
-
 // Fused Q RMSNorm + GPT-J RoPE + FP8/UE8M0 KV-cache insert (strides in BF16 elements, even).
 cudaError_t launch_qnorm_rope_kv_insert(const void *q, int64_t q_stride, void *q_out, int64_t q_out_stride,
                                         int num_tokens, int num_heads, const float *norm_w, float eps,
@@ -116,14 +103,11 @@ cudaError_t launch_topk_select(const float *scores, int64_t score_stride, int wi
                                int num_tokens, int top_k, int32_t *out, int64_t out_stride, int32_t *lens,
                                int cluster, cudaStream_t stream);
 
-cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
-cudaError_t launch_merge(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
 int decode_tc_block_keys();
 cudaError_t launch_wait_selftest(long long limit, unsigned *status, cudaStream_t stream);
 int decode_tc_table_bits(int topk_width);   // combine hash set of the tensor-core kernel: 2^bits 8-byte slots
 int decode_tc_max_splits();
 int decode_tc_resident_ctas(int splits);
-int merge_max_splits();
 
 }  // namespace dsv4

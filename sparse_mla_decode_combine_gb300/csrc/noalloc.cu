@@ -3,9 +3,9 @@
 // Some callers cannot allocate device memory at decode time: code that runs inside a
 // captured or replayed pipeline whose memory was fixed up front, plug-ins whose host
 // framework owns every allocation, or environments where cudaMalloc is not allowed
-// between set-up and shutdown.  This entry point takes the decode's scratch (the
-// combined index lists or cache slots, their lengths and the split partials) from
-// one static device array compiled into the library instead of a workspace argument.
+// between set-up and shutdown.  This entry point takes the decode's scratch (the cache
+// slots of the keys past each split's first two blocks) from one static device array
+// compiled into the library instead of a workspace argument.
 // The array is kNoAllocScratchBytes (32 MiB) and exists on every GPU that loads the
 // library until the process exits.
 #include <mutex>

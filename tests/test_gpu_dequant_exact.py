@@ -13,8 +13,8 @@ Each 128-element scale block holds half of the 254 non-NaN codes under one scale
 exponent; the exponents run from 20 to 240, so every dequantised value and every
 partial result stays a normal fp32 number (scale exponents below 20 would take values
 under 2^-116, where the fp32 accumulator itself is subnormal; they are left to the
-tolerance tests).  Both the tensor-core path (64 heads) and the CUDA-core path (16
-heads) run.
+tolerance tests).  It runs at 64 heads and at 16 heads (a 64-head group whose missing
+heads have zero queries).
 """
 import numpy as np
 import pytest
