@@ -3,7 +3,9 @@
 Tolerances (gpu_util): BF16 output max |err| <= 2e-2 and rel-L2 <= 1e-2; LSE |err| <= 1e-3.
 Small versions of the five workloads run whole; the full-size workloads run in
 the same launch configuration the benchmark times, checked on all tokens where
-the oracle is quick (1, 2, 5) and on sampled tokens otherwise (3, 4).
+the oracle is quick (1, 2, 5) and on sampled tokens otherwise (3, 4).  16 and 32
+heads (a 64-head group with zero queries for the missing heads) run the edge cases,
+the junk and widest top-k rows, and the long ragged workload at full size.
 """
 import numpy as np
 import pytest
@@ -74,6 +76,22 @@ def test_decode_full_configs_sampled_tokens(n):
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("heads", [16, 32])
+def test_decode_low_heads_full_size(heads):
+    """16 or 32 heads (one 64-head group whose missing heads have zero queries) over the long
+    ragged workload's rows: 16 tokens, histories of 1024..131072, top-k 2048, window 256,
+    Student-t latents, sinks; every token against the oracle, and nothing written past the
+    heads that exist."""
+    need_gpu()
+    w5 = full_config(5)
+    w = synth.make_workload(name=f"long-ragged h={heads}", seed=1105, heads=heads, req_seq_lens=list(w5.seq_lens),
+                            topk_width=2048, window=256, sink=True, latent_dist="t3")
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(w)
+    compare_decode(out, lse, ref_out, ref_lse, what=w.name)
+
+
 def _edge_workload(heads, sink, window=16, seqs=(1, 0, 2, 5, 300, 129, 64, 65), topk_width=40, seed=77):
     return synth.make_workload(name="edge", seed=seed, heads=heads, req_seq_lens=list(seqs), topk_width=topk_width,
                                window=window, sink=sink)
@@ -91,7 +109,7 @@ def test_decode_edge_lengths(heads, sink):
     compare_decode(out, lse, ref_out, ref_lse, what=f"edge h={heads} sink={sink}")
 
 
-@pytest.mark.parametrize("heads", [64, 128])
+@pytest.mark.parametrize("heads", [32, 64, 128])
 def test_decode_junk_topk_entries(heads):
     """Repeats (also across the 2176-entry passes of the fused combine), -1 padding, positions
     past the token, positions inside the window and a topk_lens cut, in 3000-wide top-k rows."""
@@ -119,7 +137,7 @@ def test_decode_junk_topk_entries(heads):
     compare_decode(out, lse, ref_out, ref_lse, what=f"junk top-k h={heads}")
 
 
-@pytest.mark.parametrize("heads", [64, 128])
+@pytest.mark.parametrize("heads", [32, 64, 128])
 def test_decode_max_topk_width(heads):
     """The widest top-k rows the library takes (8192 entries, the fused combine's hash set at its
     2^14-slot cap and half full) with a 1024-entry window: many repeats of a few thousand
