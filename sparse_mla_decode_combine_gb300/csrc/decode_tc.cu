@@ -1038,13 +1038,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         if (!is_mma) {
             const int S = p.splits;
             const int hp = (kNH + S - 1) / S;
-            if (wid < kNH)
+            const int nhe = min(kNH, p.num_heads - h0);   // the merge reads only the heads that exist
+            if (wid < nhe)
                 push_stat(smem_u32(gbase), S, split, wid, alpha[wid], fin[wid]);
             const uint32_t recv_s = sK;
             const int r0 = hs / hp;   // this warp's 16 heads belong to owners r0, r0 + 1, r0 + 2 at most
             uint32_t x[16];
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
+                if (hs >= nhe)   // nhe is a multiple of 16: whole warps skip
+                    break;
                 const int dv = 128 * m + key;
                 tmem_ld16(lane_base + kColO + 64 * m + hs, x);
                 tmem_ld_wait();
