@@ -14,7 +14,8 @@
 // distributed shared memory and writes the sums into every CTA; each CTA then finds the digit
 // itself (two cluster barriers a round).  Round 0 reads the scores from HBM with 16-byte loads issued four deep and keeps
 // the segment's keys in shared memory (up to 40960 keys a CTA).  One pass over the cached
-// keys then lists the keys of round 0's bin with their positions (up to 128 a warp chunk) and
+// keys then lists the keys of round 0's bin with their positions (up to 128 a warp chunk, 256 in
+// a whole-row CTA whose shared memory has room) and
 // counts the keys above it; rounds 1 and 2 and the per-chunk counts work on that list alone
 // (a segment with more candidates, i.e. many equal keys, rescans its keys instead).  The
 // compaction walks the segment in position order, one contiguous chunk per warp with warp
@@ -34,7 +35,9 @@ constexpr int kTkThreadsCluster = 512;
 constexpr int kTkBins = 2048;          // 11-bit digits
 constexpr int kTkCacheKeys = 40960;    // keys of a segment kept in shared memory (160 KB)
 constexpr int kTkStep = 32 * 8;        // compaction: a warp takes 8 consecutive positions per lane
-constexpr int kTkCandWarp = 128;       // candidates (keys in round 0's bin) a warp chunk keeps in shared memory
+constexpr int kTkCandWarp = 128;       // candidates (keys in round 0's bin) a warp chunk keeps in shared memory,
+constexpr int kTkCandWarpWide = 256;   // or, for whole-row CTAs whose shared memory has room, this many
+constexpr int kTkRowDynMax = 204800;   // dynamic shared memory of a whole-row CTA (with its 17 KB static: < 227 KB)
 
 struct TopkParams {
     const float *scores;
@@ -47,6 +50,7 @@ struct TopkParams {
     int32_t *lens;
     int32_t cluster;
     int32_t cache;   // keys of shared-memory cache per CTA (0: no cache; every segment fits otherwise)
+    int32_t cand;    // entries of a warp's candidate list (kTkCandWarp or kTkCandWarpWide)
 };
 
 // Order-preserving key: larger score -> larger key; -0 and +0 share a key; NaN -> 0, below
@@ -216,7 +220,6 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
 {
     constexpr int kTkThreads = NT;
     constexpr int kTkWarps = NT / 32;
-    constexpr int kTkCandMax = kTkCandWarp * kTkWarps;
     __shared__ uint32_t hist[kTkBins];     // this CTA's histogram of the round
     __shared__ uint32_t slice[kTkBins];    // the cluster-wide histogram (clusters of more than one CTA)
     __shared__ uint32_t bcast[2];          // the round's digit and remaining count
@@ -225,12 +228,13 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     __shared__ uint32_t wsure[kTkWarps];     // keys above round 0's bin per warp chunk
     __shared__ uint32_t wcnt[kTkWarps][2];   // (> v*, == v*) counts per warp chunk
     __shared__ uint32_t wncand[kTkWarps];    // candidates per warp chunk
-    // [p.cache keys][kTkCandMax candidate keys][kTkCandMax positions][a bit per cached position]
+    // [p.cache keys][cand x warps candidate keys][cand x warps positions][a bit per cached position]
     extern __shared__ uint4 dyn4[];
     uint32_t *kc = reinterpret_cast<uint32_t *>(dyn4);
     uint32_t *ckey = kc + p.cache;
-    uint32_t *cpos = ckey + kTkCandMax;
-    uint32_t *bm = cpos + kTkCandMax;      // the selected positions of the segment (with the cache)
+    const int cap = p.cand;                // entries of a warp's candidate list
+    uint32_t *cpos = ckey + cap * kTkWarps;
+    uint32_t *bm = cpos + cap * kTkWarps;  // the selected positions of the segment (with the cache)
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -345,8 +349,8 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     // of its chunk in position order; keys above the bin are selected whatever the later rounds
     // find: they are counted, and (with the cache) marked in the bitmap
     uint32_t sure = 0u, nw = 0u;   // per warp (the same in every lane): keys above the bin, candidates so far
-    uint32_t *wkey = ckey + warp * kTkCandWarp;
-    uint32_t *wpos = cpos + warp * kTkCandWarp;
+    uint32_t *wkey = ckey + warp * cap;
+    uint32_t *wpos = cpos + warp * cap;
     const uint32_t below = (1u << lane) - 1u;
     for (int i0 = c_lo; i0 < c_hi; i0 += 128) {   // lane l takes positions i0 + 32 j + l: a bitmap word is a ballot
         const bool full = cache && i0 + 128 <= c_hi;
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
             if (bc != 0u) {   // candidates in position order: (j, lane) is position order within the 128
                 if ((bc >> lane) & 1u) {
                     const uint32_t slot = nw + (uint32_t)__popc(bc & below);
-                    if (slot < (uint32_t)kTkCandWarp) {
+                    if (slot < (uint32_t)cap) {
                         wkey[slot] = k[j];
                         wpos[slot] = (uint32_t)i;
                     }
@@ -391,7 +395,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
     __syncthreads();
     bool listed = true;   // else (many equal keys in one chunk) the rounds rescan the segment
     for (int w = 0; w < kTkWarps; ++w)
-        listed = listed && wncand[w] <= (uint32_t)kTkCandWarp;
+        listed = listed && wncand[w] <= (uint32_t)cap;
 
     // ---- rounds 1 (next 11 bits) and 2 (last 10 bits)
 #pragma unroll 1
@@ -406,10 +410,10 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const TopkParams p)
             if ((k & pmask) == prefix)
                 atomicAdd(&hist[(k >> shift) & dmask], 1u);
         };
-        if (listed) {
-            for (int c = tid; c < kTkCandMax; c += kTkThreads)
-                if ((uint32_t)(c % kTkCandWarp) < wncand[c / kTkCandWarp])
-                    count(ckey[c]);
+        if (listed) {   // every warp its own list
+            const uint32_t nwc = wncand[warp];
+            for (uint32_t c = lane; c < nwc; c += 32)
+                count(wkey[c]);
         } else {
             visit_keys<NT>(row, lo, hi, vec, kc, cache, false, count);
         }
@@ -589,14 +593,21 @@ cudaError_t launch_topk_select(const float *scores, int64_t score_stride, int wi
     const long long seg_max = (((long long)width + cluster - 1) / cluster + 3) / 4 * 4;
     const int cache = seg_max <= kTkCacheKeys ? (int)seg_max : 0;
     const int warps = (cluster > 1 ? kTkThreadsCluster : kTkThreadsRow) / 32;
-    const int smem = 4 * cache + 8 * kTkCandWarp * warps + (cache ? 4 * ((cache + 31) / 32) : 0);
+    const int bm_bytes = cache ? 4 * ((cache + 31) / 32) : 0;
+    // whole-row CTAs take the longer candidate lists where they fit (a CTA has the SM to itself);
+    // clustered CTAs keep the short ones, so that two of them still share an SM
+    const int cand = (cluster == 1 && 4 * cache + 8 * kTkCandWarpWide * warps + bm_bytes <= kTkRowDynMax)
+                         ? kTkCandWarpWide
+                         : kTkCandWarp;
+    const int smem = 4 * cache + 8 * cand * warps + bm_bytes;
     const void *kernel = cluster > 1 ? reinterpret_cast<const void *>(topk_select_kernel<kTkThreadsCluster>)
                                      : reinterpret_cast<const void *>(topk_select_kernel<kTkThreadsRow>);
-    cudaError_t e = set_smem_once(kernel, 4 * kTkCacheKeys + 8 * kTkCandWarp * 32 + 4 * (kTkCacheKeys / 32),
+    const int smem_max = 4 * kTkCacheKeys + 8 * kTkCandWarp * 32 + 4 * (kTkCacheKeys / 32);
+    cudaError_t e = set_smem_once(kernel, cluster > 1 ? smem_max : (smem_max > kTkRowDynMax ? smem_max : kTkRowDynMax),
                                   cluster > 1 ? kAttrTopkCluster : kAttrTopk);
     if (e != cudaSuccess)
         return e;
-    TopkParams p{scores, score_stride, width, num_cand, top_k, out, out_stride, lens, cluster, cache};
+    TopkParams p{scores, score_stride, width, num_cand, top_k, out, out_stride, lens, cluster, cache, cand};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long long)num_tokens * cluster));
     cfg.blockDim = dim3(cluster > 1 ? kTkThreadsCluster : kTkThreadsRow);
