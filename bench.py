@@ -272,6 +272,15 @@ def ncu_shares():
         return None
 
 
+# workload names of the single-step benchmarks (the JSON line's config.workload; the key of their
+# committed DRAM-traffic records)
+TOPK_WORKLOADS = {"long-batch": "top-k selection: 128 tokens x 32768 candidate scores, top-k 2048",
+                  "long-decode": "top-k selection: 16 tokens x 1024..131071 candidate scores, top-k 2048"}
+COMBINE_COMPRESSED_WORKLOAD = ("compressed combine: 64 requests x 4 tokens, top-k 2048 of a 4x-compressed region, "
+                               "window 128, rows of 2304")
+INSERT_WORKLOAD = "q RMSNorm + GPT-J RoPE + FP8 KV insert: 128 tokens x 128 heads, 65536-slot cache"
+
+
 def traffic_record(kernel_key: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -646,13 +655,10 @@ def run_combine_compressed(args):
             "value": T / step_s, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int32", "data": "synthetic",
-            "config": {"workload": "compressed combine: 64 requests x 4 tokens, top-k 2048 of a 4x-compressed "
-                                   "region, window 128, rows of 2304", "tokens_per_step": T, "replicas": reps,
+            "config": {"workload": COMBINE_COMPRESSED_WORKLOAD, "tokens_per_step": T, "replicas": reps,
                        "l2": f"inputs larger than L2: {reps} rotating replicas"},
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                         "traffic": traffic_record("combine_compressed_kernel",
-                                                   "compressed combine: 64 requests x 4 tokens, top-k 2048 of a "
-                                                   "4x-compressed region, window 128, rows of 2304"),
+                         "traffic": traffic_record("combine_compressed_kernel", COMBINE_COMPRESSED_WORKLOAD),
                          "kernel": "combine_compressed_kernel",
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
                          "algorithmic_bytes_per_launch": bytes_per_step,
@@ -726,8 +732,7 @@ def run_topk_select(args):
     step_s = ms / 1e3 / steps
     hbm_peak, _, _, peak_src = peaks()
     ach = bytes_per_step / step_s / 1e9
-    desc = {"long-batch": "top-k selection: 128 tokens x 32768 candidate scores, top-k 2048",
-            "long-decode": "top-k selection: 16 tokens x 1024..131071 candidate scores, top-k 2048"}[w.name]
+    desc = TOPK_WORKLOADS[w.name]
     line = {"metric": "top-k selection query-tokens/s (bytes moved vs HBM roofline)",
             "value": T / step_s, "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
             "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -820,13 +825,11 @@ def run_qnorm_rope_insert(args):
             "value": T / step_s, "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
             "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "q RMSNorm + GPT-J RoPE + FP8 KV insert: 128 tokens x 128 heads, 65536-slot cache",
+            "config": {"workload": INSERT_WORKLOAD,
                        "tokens_per_step": T, "heads": H, "replicas": reps,
                        "l2": f"inputs larger than L2: {reps} rotating replicas"},
             "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                         "traffic": traffic_record("qnorm_rope_kv_insert_kernel",
-                                                   "q RMSNorm + GPT-J RoPE + FP8 KV insert: 128 tokens x 128 heads, "
-                                                   "65536-slot cache"),
+                         "traffic": traffic_record("qnorm_rope_kv_insert_kernel", INSERT_WORKLOAD),
                          "kernel": "qnorm_rope_kv_insert_kernel",
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
                          "algorithmic_bytes_per_launch": bytes_per_step,
