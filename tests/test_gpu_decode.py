@@ -177,6 +177,19 @@ def test_decode_window_only_and_topk_only():
     compare_decode(out, lse, r[0], r[1], what="top-k only")
 
 
+def test_decode_long_window():
+    """A 20000-key window (the window is a position range, never hashed): one token whose window
+    dwarfs its top-k (8 splits of ~2560 keys), one whose window covers its whole history (every
+    top-k entry falls inside it and is dropped), one shorter than its top-k row."""
+    need_gpu()
+    w = synth.make_workload(name="long window", seed=61, heads=64, req_seq_lens=[30000, 9000, 70], topk_width=512,
+                            window=20000, sink=True)
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(w)
+    compare_decode(out, lse, ref_out, ref_lse, what=w.name)
+
+
 def test_decode_many_tokens_no_split():
     """Enough tokens that every token runs in one worker (no merge)."""
     need_gpu()
