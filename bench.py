@@ -561,7 +561,7 @@ def run_ours(args):
             cpu = cpu_baseline(w, args.cpu_seconds)
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if H >= 64 else "f32",
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic",
                 "config": workload_config(w, {"l2": f"inputs larger than L2: {R} rotating replicas "
                                                     f"({R * bytes_per_step / 1e6:.0f} MB gathered per rotation, "

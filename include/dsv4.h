@@ -294,6 +294,36 @@ DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_token_strid
                                    dsv4_stream_t stream);
 
 /*
+ * dsv4_sparse_mla_decode_trace -- dsv4_sparse_mla_decode that also records, from inside the
+ * decode kernel, the combined index list each token was decoded over.
+ *
+ * A verification aid with no counterpart on the pages: the decode kernel combines each
+ * token's top-k row with its window itself (the combine of dsv4_combine_topk_swa_indices,
+ * vllm #43385 rocm.py, fused into the kernel's prologue); this entry point runs exactly that
+ * kernel and lets a test compare the list it built with the definition bit for bit.
+ *
+ * Arguments: those of dsv4_sparse_mla_decode, then
+ *   combined        int32 [num_tokens, combined_width], row stride combined_stride
+ *                   (>= combined_width >= topk_width + window): entries [0, L) of row t
+ *                   receive the logical positions of token t's keys in list order (the
+ *                   kept top-k entries, then the window ascending); entries from L on are
+ *                   not written.
+ *   combined_lens   int32 [num_tokens]: L of each token.
+ * The decode's out and lse are written as by dsv4_sparse_mla_decode.  Returns the codes of
+ * dsv4_sparse_mla_decode, and DSV4_ERR_INVALID_ARG for a missing or too narrow record.
+ */
+DSV4_API dsv4_status dsv4_sparse_mla_decode_trace(const void *q, int64_t q_token_stride, const void *kv_cache,
+                                                 int32_t num_blocks, int32_t page_block, const int32_t *block_table,
+                                                 int64_t bt_stride, int32_t max_blocks, int32_t num_reqs,
+                                                 const int32_t *req_idx, const int32_t *topk_idx,
+                                                 int64_t topk_stride, int32_t topk_width, const int32_t *topk_lens,
+                                                 const int32_t *seq_lens, int32_t num_tokens, int32_t num_heads,
+                                                 int32_t window, const float *sink, float softmax_scale, void *out,
+                                                 float *lse, void *workspace, size_t workspace_bytes,
+                                                 int32_t *combined, int64_t combined_stride, int32_t combined_width,
+                                                 int32_t *combined_lens, dsv4_stream_t stream);
+
+/*
  * dsv4_sparse_mla_decode_noalloc -- dsv4_sparse_mla_decode without a workspace argument.
  *
  * The pages have no counterpart to this entry point; it exists for callers that cannot

@@ -31,8 +31,8 @@ STATUS_NAMES = {0: "DSV4_OK", 1: "DSV4_ERR_INVALID_ARG", 2: "DSV4_ERR_BAD_INDEX"
 
 EXPORTED = ("dsv4_combine_topk_swa_indices", "dsv4_combine_topk_swa_indices_compressed", "dsv4_topk_select",
             "dsv4_qnorm_rope_kv_insert", "dsv4_selftest_wait_timeout",
-            "dsv4_sparse_mla_decode_workspace_size", "dsv4_sparse_mla_decode", "dsv4_sparse_mla_decode_noalloc",
-            "dsv4_get_device_status")
+            "dsv4_sparse_mla_decode_workspace_size", "dsv4_sparse_mla_decode", "dsv4_sparse_mla_decode_trace",
+            "dsv4_sparse_mla_decode_noalloc", "dsv4_get_device_status")
 
 
 class Dsv4Error(RuntimeError):
@@ -80,6 +80,9 @@ def load_library():
     lib.dsv4_sparse_mla_decode.restype = ctypes.c_int
     lib.dsv4_sparse_mla_decode.argtypes = [P, i64, P, i32, i32, P, i64, i32, i32, P, P, i64, i32, P, P, i32, i32,
                                            i32, P, ctypes.c_float, P, P, P, ctypes.c_size_t, P]
+    lib.dsv4_sparse_mla_decode_trace.restype = ctypes.c_int
+    lib.dsv4_sparse_mla_decode_trace.argtypes = [P, i64, P, i32, i32, P, i64, i32, i32, P, P, i64, i32, P, P, i32, i32,
+                                                 i32, P, ctypes.c_float, P, P, P, ctypes.c_size_t, P, i64, i32, P, P]
     lib.dsv4_sparse_mla_decode_noalloc.restype = ctypes.c_int
     lib.dsv4_sparse_mla_decode_noalloc.argtypes = [P, i64, P, i32, i32, P, i64, i32, i32, P, P, i64, i32, P, P, i32,
                                                    i32, i32, P, ctypes.c_float, P, P, P]
@@ -233,13 +236,50 @@ def dsv4_sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table:
         _stream(stream))
 
 
+def dsv4_sparse_mla_decode_trace(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                                 req_idx: Optional[torch.Tensor], topk_idx: torch.Tensor,
+                                 topk_lens: Optional[torch.Tensor], seq_lens: torch.Tensor, window: int,
+                                 sink: Optional[torch.Tensor], softmax_scale: float, out: torch.Tensor,
+                                 lse: Optional[torch.Tensor], workspace: torch.Tensor, combined: torch.Tensor,
+                                 combined_lens: torch.Tensor, stream=None) -> int:
+    """dsv4_sparse_mla_decode that also records the combined list the decode kernel built:
+    combined int32 [T, C] (C >= K + window) gets each token's positions [0, L), combined_lens
+    int32 [T] gets L (see include/dsv4.h)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv_cache, torch.uint8, "kv_cache", 3)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(req_idx, torch.int32, "req_idx", 1)
+    _need(topk_idx, torch.int32, "topk_idx", 2)
+    _need(topk_lens, torch.int32, "topk_lens", 1)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(sink, torch.float32, "sink", 1)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(lse, torch.float32, "lse", 2)
+    _need(workspace, torch.uint8, "workspace", 1)
+    _need(combined, torch.int32, "combined", 2)
+    _need(combined_lens, torch.int32, "combined_lens", 1)
+    if q.stride(1) != 576 or not kv_cache.is_contiguous() or not out.is_contiguous():
+        raise ValueError("q heads must be contiguous rows of 576; kv_cache and out must be contiguous")
+    if kv_cache.shape[2] != 656:
+        raise ValueError("kv_cache entries must be 656 bytes")
+    T, H, _ = q.shape
+    K = topk_idx.shape[1]
+    return load_library().dsv4_sparse_mla_decode_trace(
+        _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
+        block_table.stride(0), block_table.shape[1], block_table.shape[0], _ptr(req_idx),
+        _ptr(topk_idx) if K > 0 else None, max(topk_idx.stride(0), K), K, _ptr(topk_lens), _ptr(seq_lens), T, H,
+        int(window), _ptr(sink), float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _ptr(combined), max(combined.stride(0), combined.shape[1]), combined.shape[1], _ptr(combined_lens),
+        _stream(stream))
+
+
 def dsv4_sparse_mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
                                    req_idx: Optional[torch.Tensor], topk_idx: torch.Tensor,
                                    topk_lens: Optional[torch.Tensor], seq_lens: torch.Tensor, window: int,
                                    sink: Optional[torch.Tensor], softmax_scale: float, out: torch.Tensor,
                                    lse: Optional[torch.Tensor], stream=None) -> int:
     """dsv4_sparse_mla_decode for callers that cannot allocate a workspace: the library's
-    own 16 MiB static device array serves as scratch (see include/dsv4.h)."""
+    own 32 MiB static device array serves as scratch (see include/dsv4.h)."""
     _need(q, torch.bfloat16, "q", 3)
     _need(kv_cache, torch.uint8, "kv_cache", 3)
     _need(block_table, torch.int32, "block_table", 2)

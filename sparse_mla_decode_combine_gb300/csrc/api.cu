@@ -274,14 +274,17 @@ extern "C" DSV4_API size_t dsv4_sparse_mla_decode_workspace_size(int32_t num_tok
     return pl.total;
 }
 
-extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_token_stride, const void *kv_cache,
-                                              int32_t num_blocks, int32_t page_block, const int32_t *block_table,
-                                              int64_t bt_stride, int32_t max_blocks, int32_t num_reqs,
-                                              const int32_t *req_idx, const int32_t *topk_idx, int64_t topk_stride,
-                                              int32_t topk_width, const int32_t *topk_lens, const int32_t *seq_lens,
-                                              int32_t num_tokens, int32_t num_heads, int32_t window,
-                                              const float *sink, float softmax_scale, void *out, float *lse,
-                                              void *workspace, size_t workspace_bytes, dsv4_stream_t stream)
+namespace {
+
+// The decode call, with an optional record of each token's combined list (positions in list
+// order and the list length) written by the decode kernel itself.
+dsv4_status decode_call(const void *q, int64_t q_token_stride, const void *kv_cache, int32_t num_blocks,
+                        int32_t page_block, const int32_t *block_table, int64_t bt_stride, int32_t max_blocks,
+                        int32_t num_reqs, const int32_t *req_idx, const int32_t *topk_idx, int64_t topk_stride,
+                        int32_t topk_width, const int32_t *topk_lens, const int32_t *seq_lens, int32_t num_tokens,
+                        int32_t num_heads, int32_t window, const float *sink, float softmax_scale, void *out,
+                        float *lse, void *workspace, size_t workspace_bytes, int32_t *trace, int64_t trace_stride,
+                        int32_t *trace_lens, dsv4_stream_t stream)
 {
     dsv4_status st = check_combine_args(topk_idx, topk_stride, topk_width, seq_lens, num_tokens, window);
     if (st != DSV4_OK)
@@ -347,10 +350,47 @@ extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_
     p.seq_lens = seq_lens;
     p.window = window;
     p.table_bits = pl.combine_table_bits;
+    p.trace = trace;
+    p.trace_stride = trace_stride;
+    p.trace_lens = trace_lens;
 
     // one launch: the kernel combines, decodes and merges its splits
     const cudaError_t e = launch_decode_tc(p, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_token_stride, const void *kv_cache,
+                                              int32_t num_blocks, int32_t page_block, const int32_t *block_table,
+                                              int64_t bt_stride, int32_t max_blocks, int32_t num_reqs,
+                                              const int32_t *req_idx, const int32_t *topk_idx, int64_t topk_stride,
+                                              int32_t topk_width, const int32_t *topk_lens, const int32_t *seq_lens,
+                                              int32_t num_tokens, int32_t num_heads, int32_t window,
+                                              const float *sink, float softmax_scale, void *out, float *lse,
+                                              void *workspace, size_t workspace_bytes, dsv4_stream_t stream)
+{
+    return decode_call(q, q_token_stride, kv_cache, num_blocks, page_block, block_table, bt_stride, max_blocks,
+                       num_reqs, req_idx, topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens,
+                       num_heads, window, sink, softmax_scale, out, lse, workspace, workspace_bytes, nullptr, 0,
+                       nullptr, stream);
+}
+
+extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode_trace(
+    const void *q, int64_t q_token_stride, const void *kv_cache, int32_t num_blocks, int32_t page_block,
+    const int32_t *block_table, int64_t bt_stride, int32_t max_blocks, int32_t num_reqs, const int32_t *req_idx,
+    const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width, const int32_t *topk_lens,
+    const int32_t *seq_lens, int32_t num_tokens, int32_t num_heads, int32_t window, const float *sink,
+    float softmax_scale, void *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *combined,
+    int64_t combined_stride, int32_t combined_width, int32_t *combined_lens, dsv4_stream_t stream)
+{
+    if (num_tokens > 0 && (combined == nullptr || combined_lens == nullptr || combined_stride < combined_width ||
+                           (long long)combined_width < (long long)topk_width + window))
+        return DSV4_ERR_INVALID_ARG;
+    return decode_call(q, q_token_stride, kv_cache, num_blocks, page_block, block_table, bt_stride, max_blocks,
+                       num_reqs, req_idx, topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens,
+                       num_heads, window, sink, softmax_scale, out, lse, workspace, workspace_bytes, combined,
+                       combined_stride, combined_lens, stream);
 }
 
 extern "C" DSV4_API dsv4_status dsv4_get_device_status(dsv4_stream_t stream)

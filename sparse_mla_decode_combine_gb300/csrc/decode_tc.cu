@@ -661,6 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 rank += w < warp ? wsum[32 * u + w] : 0;
                 total += wsum[32 * u + w];
             }
+            if (((bal[u] >> lane) & 1u) && rank >= kbeg && rank < klim && p.trace != nullptr && group == 0)
+                p.trace[(int64_t)t * p.trace_stride + rank] = vg[u];
             if (((bal[u] >> lane) & 1u) && row_ok && rank >= kbeg && rank < klim) {
                 const int sl = slot_of_position(p, row, vg[u], bt_s, bt_cached);
                 if (rank - kbeg < kHeadSlots)
@@ -679,6 +681,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int nblocks = (nkeys + kBK - 1) / kBK;
     if (!row_ok && tid == 0 && nkeys > 0)
         atomicOr(p.status, kStatusBadIndex);
+    if (p.trace != nullptr && group == 0) {   // the window part of the list, and its length
+        for (int i = max(kbeg, total) + tid; i < kend; i += kThreads)
+            p.trace[(int64_t)t * p.trace_stride + i] = win_lo + (i - total);
+        if (split == 0 && tid == 0)
+            p.trace_lens[t] = L;
+    }
     if (row_ok) {   // the window part of this split
         for (int i = max(kbeg, total) + tid; i < kend; i += kThreads) {
             const int sl = slot_of_position(p, row, win_lo + (i - total), bt_s, bt_cached);

@@ -68,6 +68,11 @@ struct DecodeParams {
     const int32_t *seq_lens;
     int32_t window;
     int32_t table_bits;
+    // optional record of the combined list each token's CTAs used (logical positions in
+    // list order, and the list length); null in ordinary calls
+    int32_t *trace;
+    int64_t trace_stride;
+    int32_t *trace_lens;
 };
 
 // Raises a kernel's dynamic shared-memory limit to at least `bytes`, once per

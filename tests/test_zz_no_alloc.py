@@ -44,6 +44,25 @@ def test_noalloc_matches_workspace_entry_point_twice(n):
         compare_decode(out, lse, r_out, r_lse, what=f"no-alloc vs workspace ({w.name})")
 
 
+def test_noalloc_larger_batch_then_smaller():
+    """A larger batch leaves more scratch in the shared array than a smaller batch writes; the
+    smaller one must not read the leftovers.  Each result is compared with the workspace entry
+    point's on the same inputs."""
+    need_gpu()
+    for n in (5, 3, 1):
+        w = synth.small_config(n)
+        d = synth.to_device(w, "cuda")
+        ref_out, ref_lse = _outputs(w)
+        ws = pkg.workspace_for(w.num_tokens, w.num_heads, w.topk_width, w.window)
+        pkg.check(pkg.dsv4_sparse_mla_decode(out=ref_out, lse=ref_lse, workspace=ws, **d), "workspace decode")
+        out, lse = _outputs(w)
+        pkg.check(pkg.dsv4_sparse_mla_decode_noalloc(out=out, lse=lse, **d), "no-alloc decode")
+        torch.cuda.synchronize()
+        assert pkg.dsv4_get_device_status() == pkg.DSV4_OK
+        compare_decode(out, lse, ref_out.double().cpu().numpy(), ref_lse.double().cpu().numpy(),
+                       what=f"no-alloc after a larger batch ({w.name})")
+
+
 def test_noalloc_rejects_batches_beyond_the_scratch_array():
     need_gpu()
     T, H, K, W = 4096, 128, 2048, 128
