@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only --workload (the default line also times all five decode workloads)")
     ap.add_argument("--op", choices=["decode", "combine-compressed", "topk-select", "qnorm-rope-insert"],
                     default="decode", help="decode (the headline), or one of the steps around it on its own")
     ap.add_argument("--topk-workload", choices=["long-batch", "long-decode"], default="long-batch",
@@ -301,6 +303,270 @@ def traffic_record(kernel_key: str, workload: str):
     return None
 
 
+class DecodeBench:
+    """One decode workload resident on the device as R replicas at distinct addresses (cache pages,
+    block tables, queries, outputs), so that the bytes gathered over one rotation exceed 4x the
+    L2; steps replayed from CUDA graphs, CUDA events on the launching stream."""
+
+    def __init__(self, pkg, w, dev, replicas=0):
+        import torch
+        self.pkg, self.w, self.dev = pkg, w, dev
+        self.base = synth_to_device(w, dev)
+        self.T, self.H, self.K, self.W = w.num_tokens, w.num_heads, w.topk_width, w.window
+        lens = combined_lengths(w)
+        self.keys_per_step = int(lens.sum())
+        self.bytes_per_step = self.keys_per_step * KV_BYTES_PER_KEY
+        self.flops_per_step = self.keys_per_step * self.H * FLOPS_PER_KEY_HEAD
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+        cache_bytes = self.base["kv_cache"].numel()
+        R = max(2, math.ceil(4 * self.l2 / max(1, self.bytes_per_step)))
+        R = int(min(R, max(2, (24 << 30) // max(1, cache_bytes))))
+        if replicas > 0:
+            R = replicas
+        self.R = R
+        nb = self.nb = w.num_blocks
+        T, H = self.T, self.H
+        self.pool = torch.empty((R * nb, w.page, 656), dtype=torch.uint8, device=dev)
+        self.bts, self.qs, self.outs, self.lses = [], [], [], []
+        for r in range(R):
+            self.pool[r * nb:(r + 1) * nb].copy_(self.base["kv_cache"])
+            bt = self.base["block_table"]
+            self.bts.append(torch.where(bt >= 0, bt + r * nb, bt).contiguous())
+            self.qs.append(self.base["q"].clone())
+            self.outs.append(torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev))
+            self.lses.append(torch.empty((T, H), dtype=torch.float32, device=dev))
+        del self.base["kv_cache"]
+        self.ws = pkg.workspace_for(T, H, self.K, self.W, dev)
+        self.stream = torch.cuda.Stream(device=dev)
+
+    def step(self, i, stream=None):
+        r = i % self.R
+        b = self.base
+        return self.pkg.dsv4_sparse_mla_decode(self.qs[r], self.pool, self.bts[r], b["req_idx"], b["topk_idx"],
+                                               b["topk_lens"], b["seq_lens"], self.W, b["sink"], b["softmax_scale"],
+                                               self.outs[r], self.lses[r], self.ws, stream=stream)
+
+    def time(self, steps, warmup, world=1, sampler=None):
+        """Milliseconds for exactly `steps` steps (max over ranks) and the host times around them."""
+        import torch
+        import torch.distributed as dist
+        pkg = self.pkg
+        # first calls outside capture: library set-up, kernel attributes, the status word
+        for i in range(self.R):
+            pkg.check(self.step(i), "decode")
+        torch.cuda.synchronize()
+        pkg.check(pkg.dsv4_get_device_status(), "device status")
+        stream = self.stream
+
+        def capture(n_steps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n_steps):
+                    rc = self.step(i, stream)
+                    if rc != 0:
+                        raise RuntimeError(f"decode failed during capture: {rc}")
+            return g
+
+        G = self.R * max(1, math.ceil(64 / self.R))   # steps per graph: whole rotations
+        g_full = capture(G)
+        nrep, rem = divmod(steps, G)
+        g_rem = capture(rem) if rem else None
+        wrep, wrem = divmod(warmup, G)
+        g_wrem = capture(wrem) if wrem else None
+        with torch.cuda.stream(stream):
+            for _ in range(wrep):
+                g_full.replay()
+            if g_wrem is not None:
+                g_wrem.replay()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        h0 = time.time()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(nrep):
+                g_full.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        h1 = time.time()
+        if world > 1:
+            dist.barrier()
+        ms = max_over_ranks(ev0.elapsed_time(ev1), self.dev)
+        pkg.check(pkg.dsv4_get_device_status(), "device status")
+        return ms, h0, h1
+
+    def roofline(self, call_s):
+        """The decode call against max(gathered KV bytes / HBM peak, FLOPs / BF16 tensor peak)."""
+        hbm_peak, bf16_peak, _, peak_src = peaks()
+        t_hbm = self.bytes_per_step / (hbm_peak * 1e9)
+        t_tc = self.flops_per_step / (bf16_peak * 1e12)
+        if t_hbm >= t_tc:
+            ach = self.bytes_per_step / call_s / 1e9
+            r = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak}
+        else:
+            ach = self.flops_per_step / call_s / 1e12
+            r = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s", "frac": ach / bf16_peak}
+        r.update({"peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+                  "call_us": call_s * 1e6, "roofline_us": max(t_hbm, t_tc) * 1e6,
+                  "algorithmic_bytes_per_launch": self.bytes_per_step, "flops_per_launch": self.flops_per_step,
+                  "kv_gbs": self.bytes_per_step / call_s / 1e9, "tflops": self.flops_per_step / call_s / 1e12})
+        return r
+
+    def l2_note(self):
+        return (f"inputs larger than L2: {self.R} rotating replicas ({self.R * self.bytes_per_step / 1e6:.0f} MB "
+                f"gathered per rotation, L2 {self.l2 / 1e6:.0f} MB)")
+
+    def e2e(self, steps, world=1):
+        """The same step end to end through the C ABI: every step uploads its inputs (q, top-k rows,
+        lengths, block table: one packed pinned buffer per replica, one H2D copy) and reads its output
+        and LSE back (one D2H copy), decoding against the replica's cache pages, so the gathered KV
+        rotates through more than 4x the L2 as in the device-timed loop.  As in a serving loop the
+        copies run on their own streams, double-buffered, so that step i's kernel overlaps step i+1's
+        upload and step i-1's read-back; 64 steps a CUDA graph."""
+        import torch
+        import torch.distributed as dist
+        import numpy as np
+        pkg, w, dev, T, H, R = self.pkg, self.w, self.dev, self.T, self.H, self.R
+        arrays0 = {"q": np.ascontiguousarray(w.q.view(np.int16)), "topk_idx": w.topk_idx, "seq_lens": w.seq_lens}
+        if w.topk_lens is not None:
+            arrays0["topk_lens"] = w.topk_lens
+        if w.req_idx is not None:
+            arrays0["req_idx"] = w.req_idx
+        bt0 = w.block_table
+        shapes = {**{k: a.shape for k, a in arrays0.items()}, "block_table": bt0.shape}
+        nbytes = {**{k: a.nbytes for k, a in arrays0.items()}, "block_table": bt0.nbytes}
+        offs, total = {}, 0
+        for k in shapes:
+            offs[k] = total
+            total += -(-nbytes[k] // 256) * 256
+        out_bytes = T * H * 512 * 2
+        res_total = out_bytes + T * H * 4
+        h_in = []
+        for r in range(R):
+            hb = torch.zeros(total, dtype=torch.uint8).pin_memory()
+            bt = np.where(bt0 >= 0, bt0 + r * self.nb, bt0).astype(np.int32)
+            for k in shapes:
+                a = bt if k == "block_table" else arrays0[k]
+                hb[offs[k]:offs[k] + nbytes[k]].copy_(torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)))
+            h_in.append(hb)
+        d_in = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+        d_res = [torch.empty(res_total, dtype=torch.uint8, device=dev) for _ in range(2)]
+        h_res = [torch.empty(res_total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+
+        def views(j):
+            v = {}
+            for k in shapes:
+                x = d_in[j][offs[k]:offs[k] + nbytes[k]]
+                v[k] = (x.view(torch.bfloat16) if k == "q" else x.view(torch.int32)).view(shapes[k])
+            return v, d_res[j][:out_bytes].view(torch.bfloat16).view(T, H, 512), \
+                d_res[j][out_bytes:].view(torch.float32).view(T, H)
+        bufs = [views(0), views(1)]
+        stream = self.stream
+        s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer j uploaded
+        ev_done = [torch.cuda.Event() for _ in range(2)]   # the call on buffer j finished
+        ev_read = [torch.cuda.Event() for _ in range(2)]   # results of buffer j read back
+        G = 64
+
+        def e2e_step(i, first):
+            j = i & 1
+            if not first:
+                s_up.wait_event(ev_done[j])
+            with torch.cuda.stream(s_up):
+                d_in[j].copy_(h_in[i % R], non_blocking=True)
+                ev_in[j].record(s_up)
+            stream.wait_event(ev_in[j])
+            if not first:
+                stream.wait_event(ev_read[j])
+            v, d_out, d_lse = bufs[j]
+            rc = pkg.dsv4_sparse_mla_decode(v["q"], self.pool, v["block_table"], v.get("req_idx"), v["topk_idx"],
+                                            v.get("topk_lens"), v["seq_lens"], self.W, self.base["sink"],
+                                            self.base["softmax_scale"], d_out, d_lse, self.ws, stream=stream)
+            ev_done[j].record(stream)
+            s_down.wait_event(ev_done[j])
+            with torch.cuda.stream(s_down):
+                h_res[j].copy_(d_res[j], non_blocking=True)
+                ev_read[j].record(s_down)
+            if rc != 0:
+                raise RuntimeError(f"decode failed: {rc}")
+
+        def capture_e2e(n):
+            """n steps as one CUDA graph: the copy streams fork from and join back into `stream`."""
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                s_up.wait_stream(stream)
+                s_down.wait_stream(stream)
+                for i in range(n):
+                    e2e_step(i, i < 2)
+                stream.wait_stream(s_up)
+                stream.wait_stream(s_down)
+            return g
+        g_e2e = capture_e2e(G)
+        e_rep, e_rem = divmod(steps, G)
+        g_e2e_rem = capture_e2e(e_rem) if e_rem else None
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g_e2e.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(e_rep):
+                g_e2e.replay()
+            if g_e2e_rem is not None:
+                g_e2e_rem.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), dev)
+        # the last step read back replica (n - 1) % R's result: it equals the device-timed run's output there
+        n_last = e_rem if e_rem else G
+        last_buf = (n_last - 1) & 1
+        r_last = (n_last - 1) % R
+        if not torch.equal(h_res[last_buf][:out_bytes].view(torch.int16),
+                           self.outs[r_last].view(torch.int16).reshape(-1).cpu()):
+            raise RuntimeError("end-to-end output differs from the device-timed output")
+        return {"value": job_rate(T * steps, world, ems), "unit": UNIT, "h2d_bytes_per_step": total,
+                "d2h_bytes_per_step": res_total, "steps": steps,
+                "method": "per step: one pinned H2D copy of q/topk/seq_lens/block_table (packed, one buffer per cache "
+                          f"replica), the C-ABI call on that replica's pages ({R} replicas, as the device-timed loop), "
+                          "one D2H copy of out+lse; copies on their own streams, double-buffered, overlapping the "
+                          "neighbouring steps' calls; 64 steps a CUDA graph"}
+
+
+def synth_to_device(w, dev):
+    import synth
+    return synth.to_device(w, dev)
+
+
+def cpu_baseline_sample(w, seconds: float, max_tokens: int = 16):
+    """The oracle as it stands on a bounded sample of the workload: up to max_tokens tokens (all
+    heads), repeated for about `seconds`, one thread per token."""
+    import oracle
+    cores = os.cpu_count() or 1
+    toks = list(range(min(w.num_tokens, max_tokens, cores)))
+    oracle.sparse_mla_decode(w, tokens=[0], n_threads=1)     # load + warm
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.sparse_mla_decode(w, tokens=toks, n_threads=len(toks))
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": reps * len(toks) / el, "unit": UNIT, "cores": len(toks), "kind": "oracle",
+            "sample": f"{len(toks)} of {w.num_tokens} tokens x all {w.num_heads} heads, repeated {reps}x "
+                      f"({el:.1f} s, fp64, one thread per token)"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -321,239 +587,63 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     pkg.load_library()
+    props = torch.cuda.get_device_properties(dev)
 
     w = synth.config(args.workload)
-    base = synth.to_device(w, dev)
-    T, H, K, W = w.num_tokens, w.num_heads, w.topk_width, w.window
-    lens = combined_lengths(w)
-    keys_per_step = int(lens.sum())
-    bytes_per_step = keys_per_step * KV_BYTES_PER_KEY
-    flops_per_step = keys_per_step * H * FLOPS_PER_KEY_HEAD
-
-    # replicas of the whole workload at distinct addresses: gathered bytes over one rotation >= 4 x L2
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
-    cache_bytes = base["kv_cache"].numel()
-    R = max(2, math.ceil(4 * l2 / max(1, bytes_per_step)))
-    R = int(min(R, max(2, (24 << 30) // max(1, cache_bytes))))
-    if args.replicas > 0:
-        R = args.replicas
-    nb = w.num_blocks
-    pool = torch.empty((R * nb, w.page, 656), dtype=torch.uint8, device=dev)
-    bts, qs, outs, lses = [], [], [], []
-    for r in range(R):
-        pool[r * nb:(r + 1) * nb].copy_(base["kv_cache"])
-        bt = base["block_table"]
-        bts.append(torch.where(bt >= 0, bt + r * nb, bt).contiguous())
-        qs.append(base["q"].clone())
-        outs.append(torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev))
-        lses.append(torch.empty((T, H), dtype=torch.float32, device=dev))
-    del base["kv_cache"]
-    ws = pkg.workspace_for(T, H, K, W, dev)
-
-    def step(i):
-        r = i % R
-        return pkg.dsv4_sparse_mla_decode(qs[r], pool, bts[r], base["req_idx"], base["topk_idx"], base["topk_lens"],
-                                          base["seq_lens"], W, base["sink"], base["softmax_scale"], outs[r], lses[r],
-                                          ws)
-
-    # first calls outside capture: library setup, kernel attributes, correctness of the status
-    for i in range(R):
-        pkg.check(step(i), "decode")
-    torch.cuda.synchronize()
-    pkg.check(pkg.dsv4_get_device_status(), "device status")
-
-    stream = torch.cuda.Stream(device=dev)
-    torch.cuda.synchronize()
-
-    def capture(n_steps, start):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n_steps):
-                rc = step(start + i)
-                if rc != 0:
-                    raise RuntimeError(f"decode failed during capture: {rc}")
-        return g
-
-    G = R * max(1, math.ceil(64 / R))            # steps per graph: whole rotations
-    g_full = capture(G, 0)
-    nrep, rem = divmod(args.steps, G)
-    g_rem = capture(rem, 0) if rem else None
-    wrep, wrem = divmod(args.warmup, G)
-    g_wrem = capture(wrem, 0) if wrem else None
-
-    with torch.cuda.stream(stream):
-        for _ in range(wrep):
-            g_full.replay()
-        if g_wrem is not None:
-            g_wrem.replay()
-    torch.cuda.synchronize()
-
+    bench = DecodeBench(pkg, w, dev, args.replicas)
+    T = w.num_tokens
     sampler = ClockSampler(str(getattr(props, "uuid", "")))
     if rank == 0:
         sampler.start()
         time.sleep(0.5)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    h0 = time.time()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(nrep):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        ev1.record(stream)
-    torch.cuda.synchronize()
-    h1 = time.time()
-    if world > 1:
-        dist.barrier()
-    ms = ev0.elapsed_time(ev1)
+    ms, h0, h1 = bench.time(args.steps, args.warmup, world)
+    clocks = sampler.summary(h0, h1) if rank == 0 else None
+    value = job_rate(T * args.steps, world, ms)
+
+    # roofline of the decode call (one kernel that combines, decodes and merges its splits), timed with
+    # CUDA events over the timed region
+    launches_per_step = 1
+    call_s = ms / 1e3 / args.steps
+    roofline = bench.roofline(call_s)
+    decode_kernel = "decode_tc_kernel"
+    roofline.update({
+        "traffic": traffic_record(decode_kernel, w.name), "kernel": decode_kernel,
+        "timed": ("whole decode call per step (one kernel that combines, decodes and merges its splits), "
+                  "CUDA events on the launching stream over the timed region; per-kernel shares of the step are "
+                  "in ncu_shares (committed ncu launch list)"),
+        "ncu_shares": ncu_shares()})
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = bench.e2e(args.steps, world)
+    config = workload_config(w, {"l2": bench.l2_note(), "replicas": bench.R, "keys_per_step": bench.keys_per_step})
+    del bench
+    torch.cuda.empty_cache()
+
+    # every decode workload, each timed the same way (rotating replicas larger than L2), with its own
+    # roofline and a bounded oracle sample; the headline above is the mid-size decode
+    per_workload = None
+    if world == 1 and not args.no_per_workload:
+        per_workload = []
+        for n in range(1, 6):
+            wn = w if n == args.workload else synth.config(n)
+            bn = DecodeBench(pkg, wn, dev)
+            msn, a0, a1 = bn.time(args.steps, args.warmup)
+            rl = bn.roofline(msn / 1e3 / args.steps)
+            rl["traffic"] = traffic_record(decode_kernel, wn.name)
+            entry = {"workload": wn.name, "ms_per_step": msn / args.steps, "value": wn.num_tokens * args.steps / (msn / 1e3),
+                     "unit": UNIT, "steps": args.steps, "replicas": bn.R, "keys_per_step": bn.keys_per_step,
+                     "roofline": {k: rl[k] for k in ("bound", "achieved", "peak", "unit", "frac", "call_us",
+                                                     "roofline_us", "kv_gbs", "tflops", "traffic")},
+                     "clocks": sampler.summary(a0, a1) if rank == 0 else None}
+            del bn
+            torch.cuda.empty_cache()
+            if not args.no_cpu_baseline:
+                entry["cpu_baseline"] = cpu_baseline_sample(wn, 2.0)
+            per_workload.append(entry)
     if rank == 0:
         time.sleep(0.2)
         sampler.stop()
-    clocks = sampler.summary(h0, h1) if rank == 0 else None
-    ms = max_over_ranks(ms, dev)
-    value = job_rate(T * args.steps, world, ms)
-
-    # roofline of the decode call, timed with CUDA events over the timed region (64/128 heads: one
-    # kernel that combines, decodes and merges; 16/32 heads: combine, decode and merge kernels)
-    launches_per_step = 1
-    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
-    call_s = ms / 1e3 / args.steps
-    t_hbm = bytes_per_step / (hbm_peak * 1e9)
-    t_tc = flops_per_step / (bf16_peak * 1e12)
-    if t_hbm >= t_tc:
-        ach = bytes_per_step / call_s / 1e9
-        roofline = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak}
-    else:
-        ach = flops_per_step / call_s / 1e12
-        roofline = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s",
-                    "frac": ach / bf16_peak}
-    decode_kernel = "decode_tc_kernel"
-    roofline.update({
-        "traffic": traffic_record(decode_kernel, w.name),
-        "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
-        "kernel": decode_kernel,
-        "timed": ("whole decode call per step (one kernel that combines, decodes and merges its splits), "
-                  "CUDA events on the launching "
-                  "stream over the timed region; per-kernel shares of the step are in ncu_shares (committed ncu "
-                  "launch list)"),
-        "call_us": call_s * 1e6,
-        "algorithmic_bytes_per_launch": bytes_per_step, "flops_per_launch": flops_per_step,
-        "kv_gbs": bytes_per_step / call_s / 1e9, "tflops": flops_per_step / call_s / 1e12,
-        "roofline_us": max(t_hbm, t_tc) * 1e6, "ncu_shares": ncu_shares()})
-
-    # end to end through the C ABI from pinned host buffers
-    e2e = None
-    if not args.no_e2e:
-        # Every step's inputs travel in one pinned staging buffer (one H2D copy) and its results in
-        # one device buffer (one D2H copy); the call sees 256-byte aligned views of them.  As in a
-        # serving loop, copies run on their own streams, double-buffered, so that step i's kernel
-        # overlaps step i+1's upload and step i-1's read-back; events order every buffer's reuse.
-        arrays = {"q": np.ascontiguousarray(w.q.view(np.int16)), "block_table": w.block_table,
-                  "topk_idx": w.topk_idx, "seq_lens": w.seq_lens}
-        if w.topk_lens is not None:
-            arrays["topk_lens"] = w.topk_lens
-        if w.req_idx is not None:
-            arrays["req_idx"] = w.req_idx
-        offs, total = {}, 0
-        for k, a in arrays.items():
-            offs[k] = total
-            total += -(-a.nbytes // 256) * 256
-        out_bytes = T * H * 512 * 2
-        res_total = out_bytes + T * H * 4
-        h_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
-        for k, a in arrays.items():
-            h_in[offs[k]:offs[k] + a.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)))
-        d_in = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
-        d_res = [torch.empty(res_total, dtype=torch.uint8, device=dev) for _ in range(2)]
-        h_res = [torch.empty(res_total, dtype=torch.uint8).pin_memory() for _ in range(2)]
-
-        def views(j):
-            v = {}
-            for k, a in arrays.items():
-                x = d_in[j][offs[k]:offs[k] + a.nbytes]
-                v[k] = (x.view(torch.bfloat16) if k == "q" else x.view(torch.int32)).view(a.shape)
-            return v, d_res[j][:out_bytes].view(torch.bfloat16).view(T, H, 512), \
-                d_res[j][out_bytes:].view(torch.float32).view(T, H)
-        bufs = [views(0), views(1)]
-        s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer j uploaded
-        ev_done = [torch.cuda.Event() for _ in range(2)]   # the call on buffer j finished
-        ev_read = [torch.cuda.Event() for _ in range(2)]   # results of buffer j read back
-        pool0 = pool[:nb]
-        h2d = total
-        d2h = res_total
-        n_e2e = args.steps
-
-        def e2e_step(i, first):
-            j = i & 1
-            s_up.wait_event(ev_done[j]) if not first else None
-            with torch.cuda.stream(s_up):
-                d_in[j].copy_(h_in, non_blocking=True)
-                ev_in[j].record(s_up)
-            stream.wait_event(ev_in[j])
-            if not first:
-                stream.wait_event(ev_read[j])
-            v, d_out, d_lse = bufs[j]
-            rc = pkg.dsv4_sparse_mla_decode(v["q"], pool0, v["block_table"], v.get("req_idx"), v["topk_idx"],
-                                            v.get("topk_lens"), v["seq_lens"], W, base["sink"],
-                                            base["softmax_scale"], d_out, d_lse, ws, stream=stream)
-            ev_done[j].record(stream)
-            s_down.wait_event(ev_done[j])
-            with torch.cuda.stream(s_down):
-                h_res[j].copy_(d_res[j], non_blocking=True)
-                ev_read[j].record(s_down)
-            if rc != 0:
-                raise RuntimeError(f"decode failed: {rc}")
-
-        def capture_e2e(n):
-            """n steps as one CUDA graph: the copy streams fork from and join back into `stream`."""
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                s_up.wait_stream(stream)
-                s_down.wait_stream(stream)
-                for i in range(n):
-                    e2e_step(i, i < 2)
-                stream.wait_stream(s_up)
-                stream.wait_stream(s_down)
-            return g
-        G = 64
-        g_e2e = capture_e2e(G)
-        e_rep, e_rem = divmod(n_e2e, G)
-        g_e2e_rem = capture_e2e(e_rem) if e_rem else None
-        with torch.cuda.stream(stream):
-            for _ in range(2):
-                g_e2e.replay()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(e_rep):
-                g_e2e.replay()
-            if g_e2e_rem is not None:
-                g_e2e_rem.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        # the packed buffers carry the same call: its output equals the timed run's on replica 0
-        last = ((e_rem if e_rem else G) - 1) & 1
-        if not torch.equal(h_res[last][:out_bytes].view(torch.int16), outs[0].view(torch.int16).reshape(-1).cpu()):
-            raise RuntimeError("end-to-end output differs from the device-timed output")
-        ems = max_over_ranks(ems, dev)
-        e2e = {"value": job_rate(T * n_e2e, world, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "method": "per step: one pinned H2D copy of q/topk/seq_lens/block_table (packed), the C-ABI call, "
-                         "one D2H copy of out+lse; copies on their own streams, double-buffered, overlapping "
-                         "the neighbouring steps' calls; 64 steps a CUDA graph"}
-
-    pkg.check(pkg.dsv4_get_device_status(), "device status")
 
     if rank == 0:
         cpu = None
@@ -561,15 +651,10 @@ def run_ours(args):
             cpu = cpu_baseline(w, args.cpu_seconds)
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                "data": "synthetic",
-                "config": workload_config(w, {"l2": f"inputs larger than L2: {R} rotating replicas "
-                                                    f"({R * bytes_per_step / 1e6:.0f} MB gathered per rotation, "
-                                                    f"L2 {l2 / 1e6:.0f} MB)",
-                                              "replicas": R, "keys_per_step": keys_per_step}),
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
-                "clocks": clocks}
+                "clocks": clocks, "per_workload": per_workload}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
