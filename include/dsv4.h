@@ -275,7 +275,7 @@ DSV4_API size_t dsv4_sparse_mla_decode_workspace_size(int32_t num_tokens, int32_
  *   num_tokens      >= 0 (0 enqueues nothing).
  *   num_heads       16, 32, 64 or 128 (others: DSV4_ERR_UNSUPPORTED).
  *   sink            float32 [num_heads] or NULL.
- *   softmax_scale   finite.
+ *   softmax_scale   finite and >= 0 (a negative scale returns DSV4_ERR_INVALID_ARG; 0 gives uniform weights).
  *   out             BF16 [num_tokens, num_heads, 512], contiguous, 16-byte aligned.
  *   lse             float32 [num_tokens, num_heads], contiguous, or NULL.
  *   workspace       device scratch of at least dsv4_sparse_mla_decode_workspace_size(...)

@@ -291,7 +291,7 @@ dsv4_status decode_call(const void *q, int64_t q_token_stride, const void *kv_ca
         return st;
     if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128)
         return DSV4_ERR_UNSUPPORTED;
-    if (!std::isfinite(softmax_scale))
+    if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)   // the kernel's running max is taken on raw dot products
         return DSV4_ERR_INVALID_ARG;
     if (num_tokens == 0)
         return DSV4_OK;

@@ -58,7 +58,9 @@
 namespace dsv4 {
 namespace {
 
-constexpr int kThreads = 544;             // warp 0: MMA issue; warps 1-16: workers
+constexpr int kThreads = 608;             // warp 0: MMA issue; warps 1-16: workers; warps 17, 18: MMA issue
+constexpr int kSIssuerB = 17;            // S^T over column chunks 5-8 (a second accumulator)
+constexpr int kPVIssuerB = 18;           // O^T tiles 2 and 3
 constexpr int kWorkers = 512;
 constexpr int kBK = 128;                 // keys per block = MMA M
 constexpr int kNH = 64;                  // heads per CTA = MMA N
@@ -73,6 +75,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;            // S^T: 64 columns
 constexpr uint32_t kColO = 64;           // O^T: 4 tiles x 64 columns
 constexpr uint32_t kColL = 320;          // per-lane partial row sums: 64 columns
+constexpr uint32_t kColSb = 384;         // S^T over column chunks 5-8: 64 columns (added to kColS's)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int kMaxSplits = 8;            // portable cluster size
@@ -486,6 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int h0 = group * kNH;
     const int nhv = min(kNH, p.num_heads - h0);   // heads of the group that exist (16 or 32 heads: the rest are zero)
     const bool is_mma = warp == 0;
+    const bool is_worker = warp >= 1 && warp <= 16;
+    const bool is_issuer = is_mma || warp == kSIssuerB || warp == kPVIssuerB;
     const int wid = tid - 32;            // worker index 0..511 (warps 1-16)
 
     // ---- shared memory carve-up (1024-byte aligned base for the swizzled tiles)
@@ -513,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     // ---- set-up that reads no input, ahead of the wait for the previous grid: barriers, TMEM,
     // the combine's empty hash set
     if (tid == 0) {
-        mbar_init(bar_s, 1);
+        mbar_init(bar_s, 2);   // both S^T accumulators committed
         mbar_init(bar_p, kWorkers / 32);
         for (int m = 0; m < 4; ++m)
             mbar_init(bar_pv + 8 * m, 1);
@@ -569,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     for (int u = 0; u < kPassLoads; ++u)
         tv[u] = u < npass && u * kThreads + tid < n ? __ldg(trow + u * kThreads + tid) : -1;
     uint4 qv[kQLoads];
-    if (!is_mma) {
+    if (is_worker) {
 #pragma unroll
         for (int j = 0; j < kQLoads; ++j) {
             const int i = wid + kWorkers * j;
@@ -734,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int rrow = 8 * (((warp - 1) - (lane >> 2)) & 15) + (lane >> 2);
     const float c2 = p.scale * 1.4426950408889634f;      // logits in log2 units per raw dot product
 
-    if (!is_mma) {   // Q -> swizzled K-major B operand
+    if (is_worker) {   // Q -> swizzled K-major B operand
 #pragma unroll
         for (int j = 0; j < kQLoads; ++j) {
             const int i = wid + kWorkers * j;
@@ -750,43 +755,63 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);   // this warp's TMEM lanes
 
-    if (is_mma) {
+    if (is_issuer) {
         // descriptors: 128-byte swizzle; K-major S^T operands advance 32 B per 16-dim step and one
-        // column chunk per 64 dims; MN-major P.V operands advance 2 KB per 16 keys
+        // column chunk per 64 dims; MN-major P.V operands advance 2 KB per 16 keys.  Three threads
+        // issue, each its own chain (one thread issues a tcgen05.mma about every 70 cycles, more than
+        // an M128 N64 K16 product takes the tensor pipe): warp 0 S^T over chunks 0-4 and O^T tiles
+        // 0-1, warp 17 S^T over chunks 5-8 (a second accumulator, summed by the softmax), warp 18 O^T
+        // tiles 2-3.
         const uint64_t qk_a = sdesc(sK, 16, 1024);
         const uint64_t qk_b = sdesc(sQ, 16, 1024);
         const uint64_t pv_a = sdesc(sK, kChunkBytes, 1024);
         const uint64_t pv_b = sdesc(sP, 1024, 1024);   // one 64-head group along N: LBO unused, kept = SBO
+        const bool do_s = warp == 0 || warp == kSIssuerB;
+        const bool do_pv = warp == 0 || warp == kPVIssuerB;
+        const int c_lo = warp == kSIssuerB ? 5 : 0;             // S^T column chunks of this thread
+        const int c_hi = warp == kSIssuerB ? kChunks : 5;
+        const uint32_t s_col = warp == kSIssuerB ? kColSb : kColS;
+        const int m_lo = warp == kPVIssuerB ? 2 : 0;            // O^T tiles of this thread
         for (int b = 0; b < nblocks; ++b) {
             const uint32_t ph = (uint32_t)(b & 1);
             if (lane == 0) {
+                if (do_s) {
 #pragma unroll
-                for (int g = 0; g < kGroups; ++g) {
-                    mbar_wait_one(bar_grp + 8 * g, ph, flags, p.status);   // chunks of group g written
-                    tc_after();
+                    for (int g = 0; g < kGroups; ++g) {
+                        if (6 * g >= c_hi || (g == 0 ? 6 : kChunks) <= c_lo)
+                            continue;   // no chunk of this thread in group g
+                        mbar_wait_one(bar_grp + 8 * g, ph, flags, p.status);   // chunks of group g written
+                        tc_after();
 #pragma unroll
-                    for (int c = 6 * g; c < (g == 0 ? 6 : kChunks); ++c) {
-                        const uint64_t a = qk_a + (uint64_t)((c * kChunkBytes) >> 4);
-                        const uint64_t bq = qk_b + (uint64_t)((c * kQChunkBytes) >> 4);
+                        for (int c = 0; c < kChunks; ++c) {
+                            if (c < max(c_lo, 6 * g) || c >= min(c_hi, g == 0 ? 6 : kChunks))
+                                continue;
+                            const uint64_t a = qk_a + (uint64_t)((c * kChunkBytes) >> 4);
+                            const uint64_t bq = qk_b + (uint64_t)((c * kQChunkBytes) >> 4);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            umma(tmem + kColS, a + (uint64_t)(2 * k), bq + (uint64_t)(2 * k), kIdescQK,
-                                 (c | k) != 0 ? 1u : 0u);
+                            for (int k = 0; k < 4; ++k)
+                                umma(tmem + s_col, a + (uint64_t)(2 * k), bq + (uint64_t)(2 * k), kIdescQK,
+                                     (c != c_lo || k != 0) ? 1u : 0u);
+                        }
                     }
+                    umma_commit(bar_s);
                 }
-                umma_commit(bar_s);
-                mbar_wait_one(bar_p, ph, flags, p.status);   // P^T of block b written
-                tc_after();
-                const int ksteps = min(kBK / 16, (nkeys - b * kBK + 15) / 16);   // 16-key steps holding keys
+                if (do_pv) {
+                    mbar_wait_one(bar_p, ph, flags, p.status);   // P^T of block b written
+                    tc_after();
+                    const int ksteps = min(kBK / 16, (nkeys - b * kBK + 15) / 16);   // 16-key steps holding keys
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint64_t a = pv_a + (uint64_t)((2 * m * kChunkBytes) >> 4);
+                    for (int m = 0; m < 4; ++m) {
+                        if (m < m_lo || m >= m_lo + 2)
+                            continue;
+                        const uint64_t a = pv_a + (uint64_t)((2 * m * kChunkBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        if (kk < ksteps)
-                            umma(tmem + kColO + 64 * m, a + (uint64_t)(kk * 128), pv_b + (uint64_t)(kk * 128), kIdescPV,
-                                 (b > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(bar_pv + 8 * m);   // releases K chunks 2m, 2m+1 (tile 3: also P^T)
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            if (kk < ksteps)
+                                umma(tmem + kColO + 64 * m, a + (uint64_t)(kk * 128), pv_b + (uint64_t)(kk * 128),
+                                     kIdescPV, (b > 0 || kk > 0) ? 1u : 0u);
+                        umma_commit(bar_pv + 8 * m);   // releases K chunks 2m, 2m+1 (tile 3: also P^T)
+                    }
                 }
             }
             __syncwarp();
@@ -866,9 +891,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 float mine = -INFINITY;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    uint32_t sa[8];
+                    uint32_t sa[8], sb[8];
                     tmem_ld8(lane_base + kColS + hs + 8 * half, sa);
+                    tmem_ld8(lane_base + kColSb + hs + 8 * half, sb);
                     tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        sa[j] = __float_as_uint(__uint_as_float(sa[j]) + __uint_as_float(sb[j]));
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const float m = warp_max(kv ? __uint_as_float(sa[j]) : -INFINITY);
@@ -914,11 +943,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int hb = hs + 8 * half;
-                uint32_t sv[8], l[8];
+                uint32_t sv[8], sb[8], l[8];
                 tmem_ld8(lane_base + kColS + hb, sv);
+                tmem_ld8(lane_base + kColSb + hb, sb);
                 if (b > 0)
                     tmem_ld8(lane_base + kColL + hb, l);
                 tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    sv[j] = __float_as_uint(__uint_as_float(sv[j]) + __uint_as_float(sb[j]));
                 uint32_t pk[4];
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
@@ -1021,7 +1054,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         named_bar(1, kWorkers);
         // the row sums and statistics above only read this warp's own TMEM stores: they overlap
         // the last block's P.V products, which the output needs
-        mbar_wait(bar_pv + 24, (uint32_t)((nblocks - 1) & 1), flags, p.status);
+        mbar_wait(bar_pv + 8, (uint32_t)((nblocks - 1) & 1), flags, p.status);    // tiles 0-1 (warp 0)
+        mbar_wait(bar_pv + 24, (uint32_t)((nblocks - 1) & 1), flags, p.status);   // tiles 2-3 (warp 18)
         tc_after();
         if (p.splits == 1) {
             uint32_t x[16];
@@ -1043,7 +1077,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         // the split's partial goes straight from TMEM into the shared memory of each head's owner:
         // recv[split][head - owner's first head][512] in the owner's K tile region
         cluster_sync();   // every split is past its matrix products: partials may land
-        if (!is_mma) {
+        if (is_worker) {
             const int S = p.splits;
             const int hp = (kNH + S - 1) / S;
             const int nhe = min(kNH, p.num_heads - h0);   // the merge reads only the heads that exist

@@ -199,3 +199,16 @@ def test_decode_rejects_bad_arguments():
     ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
     assert pkg.dsv4_sparse_mla_decode(out=out, lse=lse, workspace=ws[1:need + 1], **d) == pkg.DSV4_ERR_INVALID_ARG
     assert pkg.dsv4_sparse_mla_decode_workspace_size(T, 48, w.topk_width, w.window) == 0
+    d_neg = {**d, "softmax_scale": -abs(w.softmax_scale)}
+    assert pkg.dsv4_sparse_mla_decode(out=out, lse=lse, workspace=ws, **d_neg) == pkg.DSV4_ERR_INVALID_ARG
+
+
+def test_decode_zero_softmax_scale_gives_uniform_weights():
+    """scale 0: every key of a token weighs the same (the sink still counts), lse = ln(L [+ e^sink])."""
+    need_gpu()
+    w = small(5)
+    w0 = synth.Workload(**{**w.__dict__, "softmax_scale": 0.0})
+    out, lse, status = run_decode(w0)
+    assert status == pkg.DSV4_OK
+    r = oracle.sparse_mla_decode(w0)
+    compare_decode(out, lse, r[0], r[1], what="softmax scale 0")

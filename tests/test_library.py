@@ -87,7 +87,7 @@ def test_host_side_argument_errors(lib):
     bad = list(good)
     bad[4] = 0
     assert ins(*bad) == pkg.DSV4_OK
-    # decode: unsupported head count, non-finite scale, missing pointers
+    # decode: unsupported head count, non-finite or negative scale, missing pointers
     args = [None, 576 * 16, None, 1, 64, None, 1, 1, 1, None, None, 0, 0, None, ctypes.c_void_p(16), 1, 16, 8, None,
             1.0, None, None, None, 0, S]
     bad = list(args)
@@ -95,6 +95,8 @@ def test_host_side_argument_errors(lib):
     assert lib.dsv4_sparse_mla_decode(*bad) == pkg.DSV4_ERR_UNSUPPORTED
     bad = list(args)
     bad[19] = float("nan")
+    assert lib.dsv4_sparse_mla_decode(*bad) == pkg.DSV4_ERR_INVALID_ARG
+    bad[19] = -0.5   # a negative scale: the running max would be taken on the wrong side
     assert lib.dsv4_sparse_mla_decode(*bad) == pkg.DSV4_ERR_INVALID_ARG
     assert lib.dsv4_sparse_mla_decode(*args) == pkg.DSV4_ERR_INVALID_ARG
     bad = list(args)
