@@ -229,6 +229,12 @@ __device__ __forceinline__ float warp_max(float v)
     return r;
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only); `bytes` < 16 fills the rest with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_stream(const void *p)
 {
     uint4 v;
@@ -549,7 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // ---- early loads: the token's sizes and top-k run first (the combine waits on them), then Q
+    // ---- early loads: the token's sizes and top-k run first (the combine waits on them), then Q,
+    // copied asynchronously into its tile (the combine works in the K tile region)
     const int seq_len = p.seq_lens[t];
     const int W = p.topk_width;
     int n = W;
@@ -573,16 +580,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
 #pragma unroll
     for (int u = 0; u < kPassLoads; ++u)
         tv[u] = u < npass && u * kThreads + tid < n ? __ldg(trow + u * kThreads + tid) : -1;
-    uint4 qv[kQLoads];
-    if (is_worker) {
+    if (is_worker) {   // Q -> swizzled K-major B operand (zeros for heads that do not exist)
 #pragma unroll
         for (int j = 0; j < kQLoads; ++j) {
             const int i = wid + kWorkers * j;
             const int h = i / (kDim / 8);
             const int c = i % (kDim / 8);
-            qv[j] = h < nhv ? ld_stream(p.q + (int64_t)t * p.q_token_stride + (int64_t)(h0 + h) * kDim + 8 * c)
-                            : make_uint4(0u, 0u, 0u, 0u);
+            cp_async16(sQ + (c >> 3) * kQChunkBytes + sw128(h, c & 7),
+                       p.q + (int64_t)t * p.q_token_stride + (int64_t)(h0 + min(h, nhv - 1)) * kDim + 8 * c,
+                       h < nhv ? 16u : 0u);
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
 
     // ---- fused combine (kept top-k entries in input order, then the window ascending):
@@ -703,6 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     }
 
     if (nblocks == 0) {   // no key in this split
+        asm volatile("cp.async.wait_all;" ::: "memory");   // the Q copy lands before the merge overlays Q
         if (is_mma) {   // TMEM back (its address is visible after the combine's barriers)
             tc_after();
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot), "r"(kTmemCols)
@@ -739,15 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int rrow = 8 * (((warp - 1) - (lane >> 2)) & 15) + (lane >> 2);
     const float c2 = p.scale * 1.4426950408889634f;      // logits in log2 units per raw dot product
 
-    if (is_worker) {   // Q -> swizzled K-major B operand
-#pragma unroll
-        for (int j = 0; j < kQLoads; ++j) {
-            const int i = wid + kWorkers * j;
-            const int h = i / (kDim / 8);
-            const int c = i % (kDim / 8);
-            st_shared_v4(sQ + (c >> 3) * kQChunkBytes + sw128(h, c & 7), qv[j].x, qv[j].y, qv[j].z, qv[j].w);
-        }
-    }
+    if (is_worker)
+        asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's Q pieces have landed
     fence_async_smem();
     tc_before();
     __syncthreads();   // slots of blocks 0/1, Q, barriers, TMEM address; the hash set is dead
