@@ -283,6 +283,14 @@ COMBINE_COMPRESSED_WORKLOAD = ("compressed combine: 64 requests x 4 tokens, top-
 INSERT_WORKLOAD = "q RMSNorm + GPT-J RoPE + FP8 KV insert: 128 tokens x 128 heads, 65536-slot cache"
 
 
+def decode_launches(w, sms: int) -> int:
+    """Kernels one decode call enqueues: the decode, plus the one-CTA ordering kernel when the
+    tokens' list lengths are given and the (token, 64-head group) units outnumber the
+    multiprocessors (the rule of the C ABI's decode call)."""
+    units = w.num_tokens * ((w.num_heads + 63) // 64)
+    return 2 if (w.topk_lens is not None and units > sms) else 1
+
+
 def traffic_record(kernel_key: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -600,15 +608,17 @@ def run_ours(args):
     clocks = sampler.summary(h0, h1) if rank == 0 else None
     value = job_rate(T * args.steps, world, ms)
 
-    # roofline of the decode call (one kernel that combines, decodes and merges its splits), timed with
-    # CUDA events over the timed region
-    launches_per_step = 1
+    # roofline of the decode call (the kernel that combines, decodes and merges its splits; for varying
+    # list lengths over many units, an ordering kernel ahead of it), timed with CUDA events over the
+    # timed region
+    launches_per_step = decode_launches(w, props.multi_processor_count)
     call_s = ms / 1e3 / args.steps
     roofline = bench.roofline(call_s)
     decode_kernel = "decode_tc_kernel"
     roofline.update({
         "traffic": traffic_record(decode_kernel, w.name), "kernel": decode_kernel,
-        "timed": ("whole decode call per step (one kernel that combines, decodes and merges its splits), "
+        "timed": ("whole decode call per step (the kernel that combines, decodes and merges its splits, after "
+                  "the one-CTA ordering kernel when the call enqueues one), "
                   "CUDA events on the launching stream over the timed region; per-kernel shares of the step are "
                   "in ncu_shares (committed ncu launch list)"),
         "ncu_shares": ncu_shares()})
@@ -633,6 +643,7 @@ def run_ours(args):
             rl["traffic"] = traffic_record(decode_kernel, wn.name)
             entry = {"workload": wn.name, "ms_per_step": msn / args.steps, "value": wn.num_tokens * args.steps / (msn / 1e3),
                      "unit": UNIT, "steps": args.steps, "replicas": bn.R, "keys_per_step": bn.keys_per_step,
+                     "launches_per_step": decode_launches(wn, props.multi_processor_count),
                      "roofline": {k: rl[k] for k in ("bound", "achieved", "peak", "unit", "frac", "call_us",
                                                      "roofline_us", "kv_gbs", "tflops", "traffic")},
                      "clocks": sampler.summary(a0, a1) if rank == 0 else None}

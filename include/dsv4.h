@@ -282,6 +282,9 @@ DSV4_API size_t dsv4_sparse_mla_decode_workspace_size(int32_t num_tokens, int32_
  *                   bytes, 256-byte aligned, not used by anything else until the work
  *                   enqueued by this call has finished.  Its contents on entry do not matter.
  *   stream          CUDA stream.
+ * When topk_lens is given and num_tokens * ceil(num_heads / 64) exceeds the device's
+ * multiprocessor count, the call enqueues a one-CTA ordering kernel ahead of the decode kernel,
+ * so that the tokens with the longest lists start first; the results do not depend on it.
  * Returns DSV4_OK, DSV4_ERR_INVALID_ARG, DSV4_ERR_UNSUPPORTED or DSV4_ERR_CUDA.
  */
 DSV4_API dsv4_status dsv4_sparse_mla_decode(const void *q, int64_t q_token_stride, const void *kv_cache, int32_t num_blocks,

@@ -103,6 +103,8 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
     size_t off = 0;
     p.off_combined = off;
     off = align_up(off + sizeof(int32_t) * (size_t)num_tokens * (size_t)p.cw, 256);
+    p.off_order = off;   // the units' launch order, when the call needs one
+    off = align_up(off + sizeof(int32_t) * (size_t)num_tokens * (size_t)p.groups, 256);
     p.total = std::max<size_t>(off, 256);
     *pl = p;
     return true;
@@ -353,6 +355,12 @@ dsv4_status decode_call(const void *q, int64_t q_token_stride, const void *kv_ca
     p.trace = trace;
     p.trace_stride = trace_stride;
     p.trace_lens = trace_lens;
+    // Lists of different lengths over more (token, head group) units than multiprocessors: the
+    // units start longest first (a one-CTA ordering kernel runs ahead of the decode).  Equal
+    // lengths gain nothing from it.
+    p.order = nullptr;
+    if (topk_lens != nullptr && (long long)num_tokens * pl.groups > sms)
+        p.order = reinterpret_cast<int32_t *>(ws + pl.off_order);
 
     // one launch: the kernel combines, decodes and merges its splits
     const cudaError_t e = launch_decode_tc(p, reinterpret_cast<cudaStream_t>(stream));

@@ -488,12 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int unit = blockIdx.x;
-    const int split = unit % p.splits;   // = rank in the cluster when splits > 1
-    const int group = (unit / p.splits) % p.groups;
-    const int t = unit / (p.splits * p.groups);
-    const int h0 = group * kNH;
-    const int nhv = min(kNH, p.num_heads - h0);   // heads of the group that exist (16 or 32 heads: the rest are zero)
+    const int split = blockIdx.x % p.splits;   // = rank in the cluster when splits > 1
     const bool is_mma = warp == 0;
     const bool is_worker = warp >= 1 && warp <= 16;
     const bool is_issuer = is_mma || warp == kSIssuerB || warp == kPVIssuerB;
@@ -554,6 +549,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     // scheduled now (it waits for this grid's results itself)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // this cluster's (token, head group): the ordering kernel's choice, else index order
+    const int cl = blockIdx.x / p.splits;
+    const int unit = p.order != nullptr ? p.order[cl] : cl;
+    const int group = unit % p.groups;
+    const int t = unit / p.groups;
+    const int h0 = group * kNH;
+    const int nhv = min(kNH, p.num_heads - h0);   // heads of the group that exist (16 or 32 heads: the rest are zero)
 
     // ---- early loads: the token's sizes and top-k run first (the combine waits on them), then Q,
     // copied asynchronously into its tile (the combine works in the K tile region)
@@ -1121,6 +1124,67 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     }
 }
 
+// Launch order of the (token, head group) units for calls whose per-token lists vary in length
+// and whose CTAs span more than one wave: CTAs start in index order as multiprocessors free up,
+// so giving the units with the longest lists the first indices lets the short ones fill the
+// tail (greedy longest-first scheduling).  The key is the estimated number of 128-key blocks
+// of the token's list (its top-k length, at most the positions before the window, plus the
+// window); one CTA counting-sorts the units by it, descending.  Units with equal keys may come
+// in any order: a unit's result does not depend on which CTA computes it.
+constexpr int kOrderThreads = 1024;
+
+__device__ __forceinline__ int order_key(const int32_t *topk_lens, const int32_t *seq_lens, int t, int topk_width,
+                                         int window)
+{
+    const int seq = seq_lens[t];
+    int n = topk_lens != nullptr ? topk_lens[t] : topk_width;
+    n = n < 0 ? 0 : (n > topk_width ? topk_width : n);
+    const int swa = seq > 0 ? min(window, seq) : 0;
+    const long long est = (long long)min(n, max(seq - swa, 0)) + swa;
+    const long long blocks = (est + kBK - 1) / kBK;
+    return (int)(blocks < kOrderThreads - 1 ? blocks : kOrderThreads - 1);
+}
+
+__global__ void __launch_bounds__(kOrderThreads) decode_order_kernel(const int32_t *topk_lens, const int32_t *seq_lens,
+                                                                     int num_tokens, int topk_width, int window,
+                                                                     int groups, int32_t *order)
+{
+    __shared__ int cnt[kOrderThreads];
+    __shared__ int wsum[kOrderThreads / 32];
+    const int tid = threadIdx.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the lengths may come from the previous kernel
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the decode waits for this grid itself
+    cnt[tid] = 0;
+    __syncthreads();
+    const int units = num_tokens * groups;
+    for (int u = tid; u < units; u += kOrderThreads)
+        atomicAdd(&cnt[order_key(topk_lens, seq_lens, u / groups, topk_width, window)], 1);
+    __syncthreads();
+    // start[k] = number of units with a larger key: an inclusive scan of the counts in
+    // descending key order (thread i holds key kOrderThreads - 1 - i), minus the own count
+    const int k = kOrderThreads - 1 - tid;
+    const int c = cnt[k];
+    int v = c;
+    const int lane = tid & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d)
+            v += y;
+    }
+    if (lane == 31)
+        wsum[tid >> 5] = v;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < (tid >> 5); ++w)
+        before += wsum[w];
+    __syncthreads();
+    cnt[k] = before + v - c;
+    __syncthreads();
+    for (int u = tid; u < units; u += kOrderThreads)
+        order[atomicAdd(&cnt[order_key(topk_lens, seq_lens, u / groups, topk_width, window)], 1)] = u;
+}
+
 // Self-test of the bounded waits: one thread waits, at most `limit` SM cycles, on an mbarrier
 // that nothing arrives on; the wait gives up, sets the abort flag and the timeout bit, and the
 // kernel ends normally.
@@ -1206,6 +1270,21 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
     cudaError_t e = set_smem_once(reinterpret_cast<const void *>(decode_tc_kernel), kSmemBytes, kAttrTc);
     if (e != cudaSuccess)
         return e;
+    if (p.order != nullptr) {   // the launch order, ahead of the decode (which waits for it)
+        cudaLaunchConfig_t ocfg = {};
+        ocfg.gridDim = dim3(1);
+        ocfg.blockDim = dim3(kOrderThreads);
+        ocfg.stream = stream;
+        cudaLaunchAttribute oattr[1];
+        oattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        oattr[0].val.programmaticStreamSerializationAllowed = 1;
+        ocfg.attrs = oattr;
+        ocfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&ocfg, decode_order_kernel, p.topk_lens, p.seq_lens, p.num_tokens, p.topk_width,
+                               p.window, p.groups, p.order);
+        if (e != cudaSuccess)
+            return e;
+    }
     const long long grid = (long long)p.num_tokens * p.groups * p.splits;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);

@@ -33,7 +33,7 @@ struct Plan {
     int chunk;             // combined-list entries per split
     int cw;                // row width of the workspace's slot rows (topk_width + window)
     int combine_table_bits;
-    size_t off_combined, total;
+    size_t off_combined, off_order, total;
 };
 
 struct DecodeParams {
@@ -73,6 +73,9 @@ struct DecodeParams {
     int32_t *trace;
     int64_t trace_stride;
     int32_t *trace_lens;
+    // launch order of the (token, head group) units, longest estimated list first, written by
+    // the ordering kernel ahead of the decode; null: index order
+    int32_t *order;
 };
 
 // Raises a kernel's dynamic shared-memory limit to at least `bytes`, once per

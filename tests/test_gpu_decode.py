@@ -6,6 +6,8 @@ the same launch configuration the benchmark times, checked on every token.  16 a
 heads (a 64-head group with zero queries for the missing heads) run the edge cases,
 the junk and widest top-k rows, and the long ragged workload at full size.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -149,6 +151,33 @@ def test_decode_many_tokens_no_split():
     rows = np.arange(0, 400, 7)
     r = oracle.sparse_mla_decode(w, tokens=rows)
     compare_decode(out, lse, r[0], r[1], rows=rows, what="many tokens")
+
+
+@pytest.mark.parametrize("heads,reqs,tpr", [(128, 80, 2), (16, 200, 1), (64, 120, 2)])
+def test_decode_longest_first_launch_order(heads, reqs, tpr):
+    """Per-token list lengths that vary (topk_lens given, some rows empty) over more CTAs than
+    one wave: the call orders the units longest first before the decode.  Every token and head
+    against the oracle (a unit skipped or run twice would leave or corrupt rows), and the
+    result identical to the same call on a copy of the batch without topk_lens but with the
+    rows cut at the same lengths (index order)."""
+    need_gpu()
+    rng = np.random.default_rng(77 + heads)
+    seqs = rng.integers(150, 3000, size=reqs)
+    counts = rng.integers(0, 300, size=reqs * tpr)
+    counts[::17] = 0
+    w = synth.make_workload(name=f"ordered h={heads}", seed=400 + heads, heads=heads, req_seq_lens=seqs,
+                            tokens_per_req=tpr, topk_width=300, topk_counts=counts, window=32, sink=True,
+                            pass_topk_lens=True)
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(w)
+    compare_decode(out, lse, ref_out, ref_lse, what=w.name)
+    # the same lists given without topk_lens (entries past each length are -1): index order
+    w2 = dataclasses.replace(w, topk_lens=None)
+    out2, lse2, status2 = run_decode(w2)
+    assert status2 == pkg.DSV4_OK
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
 
 
 def test_decode_padded_q_rows_and_repeat_determinism():
