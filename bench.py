@@ -409,6 +409,36 @@ class DecodeBench:
         pkg.check(pkg.dsv4_get_device_status(), "device status")
         return ms, h0, h1
 
+    def isolated(self, calls=40):
+        """Latency of one call on its own: L2 flushed (a write larger than L2) before each call, the
+        call issued directly (no graph, no neighbouring call to overlap its prologue with), CUDA
+        events around it on its stream after a GPU-side pause that lets the host queue the call
+        first. Median and minimum in microseconds."""
+        import torch
+        pkg = self.pkg
+        stream = self.stream
+        flush = torch.empty(2 * self.l2, dtype=torch.uint8, device=self.dev)
+        times = []
+        for i in range(calls):
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                flush.fill_(i & 0xFF)
+                # the GPU idles ~0.5 ms before the first event, so that the call is already queued
+                # when it starts: the events time the GPU, not the host's launch
+                torch.cuda._sleep(1_000_000)
+                ev0.record(stream)
+                pkg.check(self.step(i % self.R, stream), "decode")
+                ev1.record(stream)
+            torch.cuda.synchronize()
+            times.append(ev0.elapsed_time(ev1) * 1e3)
+        del flush
+        pkg.check(pkg.dsv4_get_device_status(), "device status")
+        times.sort()
+        return {"median_us": times[len(times) // 2], "min_us": times[0], "calls": calls,
+                "method": "one C-ABI call at a time, L2 flushed before each, CUDA events around the call on its "
+                          "stream (queued behind a GPU-side pause so that the host's launch is not timed)"}
+
     def roofline(self, call_s):
         """The decode call against max(gathered KV bytes / HBM peak, FLOPs / BF16 tensor peak)."""
         hbm_peak, bf16_peak, _, peak_src = peaks()
@@ -626,6 +656,7 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e = bench.e2e(args.steps, world)
+    isolated = bench.isolated() if rank == 0 else None
     config = workload_config(w, {"l2": bench.l2_note(), "replicas": bench.R, "keys_per_step": bench.keys_per_step})
     del bench
     torch.cuda.empty_cache()
@@ -665,7 +696,7 @@ def run_ours(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
-                "clocks": clocks, "per_workload": per_workload}
+                "clocks": clocks, "isolated_call": isolated, "per_workload": per_workload}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
