@@ -180,6 +180,39 @@ def test_decode_longest_first_launch_order(heads, reqs, tpr):
     assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
 
 
+def test_decode_launch_order_many_units_and_odd_lengths():
+    """The ordering kernel over more units than its 1024 threads, with top-k lengths below 0 and
+    above the row width (clamped), empty histories and single keys; every token against the
+    oracle, and the no-alloc entry point (whose static scratch holds the order too) bit-identical
+    to the workspace call."""
+    need_gpu()
+    rng = np.random.default_rng(3131)
+    T = 1300
+    seqs = rng.integers(0, 400, size=T)
+    seqs[::11] = 0
+    seqs[5::13] = 1
+    counts = rng.integers(0, 48, size=T)
+    w = synth.make_workload(name="ordered many", seed=3132, heads=16, req_seq_lens=np.maximum(seqs, 1),
+                            topk_width=48, topk_counts=counts, window=8, sink=True, pass_topk_lens=True)
+    w.seq_lens[seqs == 0] = 0
+    lens = counts.astype(np.int32).copy()
+    lens[::7] = -5
+    lens[3::7] = 60
+    w = dataclasses.replace(w, topk_lens=lens)
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(w)
+    compare_decode(out, lse, ref_out, ref_lse, what=w.name)
+    d = synth.to_device(w, "cuda")
+    out2 = torch.full_like(out, 3.0)
+    lse2 = torch.full_like(lse, 3.0)
+    pkg.check(pkg.dsv4_sparse_mla_decode_noalloc(out=out2, lse=lse2, **d), "no-alloc decode")
+    torch.cuda.synchronize()
+    assert pkg.dsv4_get_device_status() == pkg.DSV4_OK
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+
+
 def test_decode_padded_q_rows_and_repeat_determinism():
     need_gpu()
     w = small(2)
