@@ -12,6 +12,7 @@ import dataclasses
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import synth
@@ -71,3 +72,32 @@ def test_decode_random_draws(seed):
     ref_out, ref_lse, bad = oracle.sparse_mla_decode(w)
     assert bad == 0
     compare_decode(out, lse, ref_out, ref_lse, what=w.name)
+
+
+@pytest.mark.parametrize("seed", list(range(7100, 7112)))
+def test_decode_random_layouts(seed):
+    """The same kind of draws with the top-k and block-table rows inside wider buffers (junk in
+    the padding, which must not be read), and without the LSE output: the output bit-identical
+    to the contiguous call's."""
+    need_gpu()
+    w = draw(seed)
+    rng = np.random.default_rng(seed + 1)
+    d = synth.to_device(w, "cuda")
+    T, H = w.num_tokens, w.num_heads
+    ws = pkg.workspace_for(T, H, w.topk_width, w.window)
+    ref = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    ref_lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    pkg.check(pkg.dsv4_sparse_mla_decode(out=ref, lse=ref_lse, workspace=ws, **d), "decode")
+    K = w.topk_width
+    tk = torch.full((T, K + int(rng.integers(1, 40))), 7, dtype=torch.int32, device="cuda")
+    tk[:, :K] = d["topk_idx"]
+    bt0 = d["block_table"]
+    bt = torch.full((bt0.shape[0], bt0.shape[1] + int(rng.integers(1, 9))), -5, dtype=torch.int32, device="cuda")
+    bt[:, :bt0.shape[1]] = bt0
+    d2 = dict(d, topk_idx=tk[:, :K], block_table=bt[:, :bt0.shape[1]])
+    assert d2["topk_idx"].stride(0) > K and d2["block_table"].stride(0) > bt0.shape[1]
+    out = torch.full((T, H, 512), 3.0, dtype=torch.bfloat16, device="cuda")
+    pkg.check(pkg.dsv4_sparse_mla_decode(out=out, lse=None, workspace=ws, **d2), "decode, strided rows, no lse")
+    torch.cuda.synchronize()
+    assert pkg.dsv4_get_device_status() == pkg.DSV4_OK
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), w.name
