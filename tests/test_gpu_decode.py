@@ -213,6 +213,32 @@ def test_decode_launch_order_many_units_and_odd_lengths():
     assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
 
 
+def test_decode_launch_order_with_split_clusters():
+    """Varying lengths up to the widest top-k row over more units than multiprocessors, long
+    enough that the planner splits every token over a cluster: the ordered units start as whole
+    clusters.  Sampled tokens (the longest, the shortest and others) against the oracle, and the
+    whole result bit-identical to the same lists in index order."""
+    need_gpu()
+    rng = np.random.default_rng(5150)
+    T = 160
+    seqs = rng.integers(9000, 20000, size=T)
+    counts = rng.integers(0, 8193, size=T)
+    counts[:4] = [0, 1, 8192, 5000]
+    w = synth.make_workload(name="ordered clusters", seed=5151, heads=16, req_seq_lens=seqs, topk_width=8192,
+                            topk_counts=counts, window=128, sink=True, pass_topk_lens=True)
+    out, lse, status = run_decode(w)
+    assert status == pkg.DSV4_OK
+    rows = np.unique(np.concatenate([np.arange(4), [int(np.argmax(counts)), int(np.argmin(counts))],
+                                     rng.choice(T, size=10, replace=False)]))
+    r = oracle.sparse_mla_decode(w, tokens=rows)
+    compare_decode(out, lse, r[0], r[1], rows=rows, what=w.name)
+    w2 = dataclasses.replace(w, topk_lens=None)
+    out2, lse2, status2 = run_decode(w2)
+    assert status2 == pkg.DSV4_OK
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+
+
 def test_decode_padded_q_rows_and_repeat_determinism():
     need_gpu()
     w = small(2)
