@@ -805,16 +805,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                     mbar_wait_one(bar_p, ph, flags, p.status);   // P^T of block b written
                     tc_after();
                     const int ksteps = min(kBK / 16, (nkeys - b * kBK + 15) / 16);   // 16-key steps holding keys
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        if (m < m_lo || m >= m_lo + 2)
-                            continue;
+                    // loops kept rolled: a small issuer body is fetched faster (instruction fetch is
+                    // the kernel's main stall, and a CTA runs this code only once a block)
+#pragma unroll 1
+                    for (int m = m_lo; m < m_lo + 2; ++m) {
                         const uint64_t a = pv_a + (uint64_t)((2 * m * kChunkBytes) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk)
-                            if (kk < ksteps)
-                                umma(tmem + kColO + 64 * m, a + (uint64_t)(kk * 128), pv_b + (uint64_t)(kk * 128),
-                                     kIdescPV, (b > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll 1
+                        for (int kk = 0; kk < ksteps; ++kk)
+                            umma(tmem + kColO + 64 * m, a + (uint64_t)(kk * 128), pv_b + (uint64_t)(kk * 128),
+                                 kIdescPV, (b > 0 || kk > 0) ? 1u : 0u);
                         umma_commit(bar_pv + 8 * m);   // releases K chunks 2m, 2m+1 (tile 3: also P^T)
                     }
                 }
