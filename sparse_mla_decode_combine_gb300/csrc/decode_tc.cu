@@ -167,11 +167,10 @@ __device__ __noinline__ void mbar_wait_one(uint32_t bar, uint32_t parity, volati
 }
 
 // Warp-wide wait: lane 0 polls, the warp then proceeds together.
+// Every lane of a warp waits itself (no hand-off from one polling lane through __syncwarp).
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *status)
 {
-    if ((threadIdx.x & 31) == 0)
-        mbar_wait_one(bar, parity, abort_flag, status);
-    __syncwarp();
+    mbar_wait_one(bar, parity, abort_flag, status);
 }
 
 __device__ __forceinline__ void named_bar(int id, int count)
@@ -911,7 +910,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 if (lane < 16)
                     redb[quad * kNH + hs + lane] = mine;
             }
-            named_bar(1, kWorkers);
+            // only the four warps of these 16 heads exchange maxima: one 128-thread barrier each
+            named_bar(2 + ((warp - 1) >> 2), 128);
             // every warp forms the block maxima of its own 16 heads (lane j and j + 16: head hs + j);
             // the four warps sharing the heads compute the same values, so the running max stays in
             // registers and the rescale decision is per warp
