@@ -972,18 +972,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 tmem_st8(lane_base + kColL + hb, l);
                 st_shared_v4(sP + sw128(key, hb >> 3), pk[0], pk[1], pk[2], pk[3]);
             }
-            if (lane < 8 && b + 2 < nblocks) {
+            if (lane < 8 && b + 2 < nblocks)
                 slots[((b + 2) % 3) * kBK + ns] = next_slot;   // read after the next softmax barrier
-                if (next_slot >= 0)   // warm L2 for block b + 2 (its register loads are issued in block b + 1)
-                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.kv + (int64_t)next_slot * kEntryBytes),
-                                 "r"((uint32_t)kEntryBytes) : "memory");
-            }
             tmem_st_wait();
             fence_async_smem();
             tc_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar_p);
+            // warm L2 for block b + 2 (its register loads are issued in block b + 1), after the hand-off
+            // of P: the issuing thread waits on the prefetch
+            if (lane < 8 && b + 2 < nblocks && next_slot >= 0)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.kv + (int64_t)next_slot * kEntryBytes),
+                             "r"((uint32_t)kEntryBytes) : "memory");
         }
 
         if (quad == 0 && lane < 16)
