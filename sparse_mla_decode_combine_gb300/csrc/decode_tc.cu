@@ -18,11 +18,14 @@
 //   O^T[128 dv x 64 heads] += V^T[128 dv x 128 keys] . P^T        (A = K tile, MN-major)
 // One BF16 K tile in shared memory (128-byte swizzle, 8-row atoms, nine 64-dim column
 // chunks) is read by both: as K-major A for S^T and, without a copy, as MN-major A for O^T.
-// S^T, O^T (four 128-dv tiles) and per-lane partial row sums live in TMEM (512 columns).
+// S^T (two accumulators over column chunks 0-4 and 5-8, summed by the softmax), O^T (four
+// 128-dv tiles) and per-lane partial row sums live in TMEM (448 of 512 columns).
 //
-// CTA = 17 warps, one (token, 64-head group, split): warp 0 issues the MMAs, warps 1-16 do
-// everything else.  A token with 16 or 32 heads is one group whose missing heads have zero
-// queries: their columns of the products are computed and dropped, never written out.  Prologue: the CTA combines its token's top-k row with the window
+// CTA = 19 warps, one (token, 64-head group, split): lane 0 of warps 0, 17 and 18 issue the
+// MMAs (warp 0: S^T over chunks 0-4 and O^T tiles 0-1; warp 17: S^T over chunks 5-8; warp 18:
+// O^T tiles 2-3), warps 1-16 do everything else.  A token with 16 or 32 heads is one group
+// whose missing heads have zero queries: their columns of the products are computed and
+// dropped, never written out.  Prologue: the CTA combines its token's top-k row with the window
 // (shared-memory hash set for first occurrences, ballot scan for the output order), keeps the
 // entries of its own split and resolves them through the block-table row (cached in shared
 // memory) to cache slots: blocks 0 and 1 straight into shared memory, later blocks into the
@@ -32,8 +35,8 @@
 //             in registers (loaded during the previous block) and writes the exact BF16
 //             values chunk by chunk; chunk c of block b+1 is written as soon as the P.V
 //             product of block b has released it; rows past the split's keys are zeros
-//   S^T       lane 0 of warp 0 issues the MMAs of column chunks 0-5 once every worker warp
-//             has written them, then those of chunks 6-8, so the product trails the dequant
+//   S^T       the MMAs of column chunks 0-5 are issued once every worker warp has written
+//             them, those of chunks 6-8 after, so the product trails the dequant
 //   softmax   all 16 warps: warp w reads TMEM lanes 32 (w % 4).. (its keys) for heads
 //             16 ((w - 1) / 4)..; per-head block maxima with redux.sync, one barrier to share
 //             them between the four warps of a head slice, which then each keep the running
@@ -166,8 +169,8 @@ __device__ __noinline__ void mbar_wait_one(uint32_t bar, uint32_t parity, volati
     }
 }
 
-// Warp-wide wait: lane 0 polls, the warp then proceeds together.
-// Every lane of a warp waits itself (no hand-off from one polling lane through __syncwarp).
+// Warp-wide wait: every lane of the warp waits itself (measured faster than one polling lane
+// handing over through __syncwarp).
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *status)
 {
     mbar_wait_one(bar, parity, abort_flag, status);
