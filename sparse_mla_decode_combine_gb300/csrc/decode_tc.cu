@@ -484,6 +484,9 @@ __device__ __forceinline__ unsigned hash_insert(unsigned long long *tab, int bit
     }
 }
 
+// kRide: the next block's entries are loaded chunk by chunk during the dequant (worth it when a CTA
+// runs many blocks), instead of in one burst after it.
+template <bool kRide>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -851,10 +854,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 const uint32_t x7 = (uint32_t)(rrow & 7);
                 const uint32_t u0 = (((uint32_t)(2 * qtr)) ^ x7) << 4;
                 const uint32_t u1 = (((uint32_t)(2 * qtr + 1)) ^ x7) << 4;
+                const uint8_t *enext = p.kv;   // kRide: the next block's entry of row rrow
+                bool ok_next = false;
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
                     if (b > 0 && c < 8 && (c & 1) == 0)
                         mbar_wait(bar_pv + 8 * (c >> 1), ph ^ 1u, flags, p.status);   // P.V of block b-1 released it
+                    if (kRide && c == 0 && b + 1 < nblocks) {   // (after the first wait: the slots of b + 1 are visible)
+                        const int sidx = slots[((b + 1) % 3) * kBK + rrow];
+                        ok_next = sidx >= 0;
+                        enext = p.kv + (int64_t)max(sidx, 0) * kEntryBytes;
+                    }
                     const uint32_t cb = rb + (uint32_t)c * kChunkBytes;
                     if (!pre_ok) {
                         const uint32_t ua = c < 8 ? u0 : ((((uint32_t)qtr) ^ x7) << 4);
@@ -868,6 +878,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                         st_shared_v4(cb + ((((uint32_t)qtr + 4u) ^ x7) << 4), pre[9].x, pre[9].y, pre[9].z,
                                      pre[9].w);
                     }
+                    if (kRide && ok_next) {   // the next block's pieces of this chunk take the registers just used
+                        if (c < 8) {
+                            pre[c] = ld_stream(enext + 64 * c + 16 * qtr);
+                        } else {
+                            pre[8] = ld_stream(enext + kRopeOffset + 16 * qtr);
+                            pre[9] = ld_stream(enext + kRopeOffset + 64 + 16 * qtr);
+                        }
+                    }
                     if (c == 5 || c == kChunks - 1) {
                         fence_async_smem();
                         __syncwarp();
@@ -875,9 +893,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                             mbar_arrive(bar_grp + 8 * (c == 5 ? 0 : 1));
                     }
                 }
+                if (kRide) {
+                    if (ok_next)   // the next block's scale word, once this block's scales are used
+                        pre_sw = __ldg(reinterpret_cast<const unsigned *>(enext + kScaleOffset));
+                    pre_ok = ok_next;
+                }
             }
-            // ---- next block's entries into registers; cache slots of block b + 2 (stored below)
-            if (b + 1 < nblocks)
+            // ---- next block's entries into registers (in one burst unless they rode along); cache
+            // slots of block b + 2 (stored below)
+            if (!kRide && b + 1 < nblocks)
                 issue_loads(b + 1);
             // cache slots of block b + 2: eight per worker warp (lanes 0-7), spread over all warps
             const int ns = 8 * (warp - 1) + lane;
@@ -1226,7 +1250,7 @@ int decode_tc_resident_ctas(int splits)
         return 0;
     if (cache[dev][splits] > 0)
         return cache[dev][splits];
-    if (set_smem_once(reinterpret_cast<const void *>(decode_tc_kernel), kSmemBytes, kAttrTc) != cudaSuccess)
+    if (set_smem_once(reinterpret_cast<const void *>(decode_tc_kernel<false>), kSmemBytes, kAttrTc) != cudaSuccess)
         return 0;
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1244,7 +1268,7 @@ int decode_tc_resident_ctas(int splits)
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(decode_tc_kernel), &cfg) !=
+        if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(decode_tc_kernel<false>), &cfg) !=
             cudaSuccess) {
             cudaGetLastError();
             return 0;
@@ -1270,7 +1294,11 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
     if (p.heads_per_group != kNH || p.num_heads < 1 || p.chunk <= 0 || p.splits < 1 || p.splits > kMaxSplits || p.topk_width < 0 ||
         p.topk_width > kMaxTopkWidth || p.table_bits < 1 || p.table_bits > kHashBitsMax)
         return cudaErrorInvalidValue;
-    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(decode_tc_kernel), kSmemBytes, kAttrTc);
+    // CTAs of more than three blocks load the next block's entries during the dequant
+    const bool ride = p.chunk > 3 * kBK;
+    const void *kernel = ride ? reinterpret_cast<const void *>(decode_tc_kernel<true>)
+                              : reinterpret_cast<const void *>(decode_tc_kernel<false>);
+    cudaError_t e = set_smem_once(kernel, kSmemBytes, ride ? kAttrTcLong : kAttrTc);
     if (e != cudaSuccess)
         return e;
     if (p.order != nullptr) {   // the launch order, ahead of the decode (which waits for it)
@@ -1304,7 +1332,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = p.splits > 1 ? 2 : 1;
     void *args[] = {const_cast<DecodeParams *>(&p)};
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(decode_tc_kernel), args);
+    return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 
 }  // namespace dsv4

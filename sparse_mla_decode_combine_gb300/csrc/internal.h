@@ -81,7 +81,7 @@ struct DecodeParams {
 // Raises a kernel's dynamic shared-memory limit to at least `bytes`, once per
 // (device, kernel slot); later calls with no larger size touch no CUDA state, so a
 // call made after the first one on a device is safe inside stream capture.
-enum AttrSlot { kAttrCombine = 0, kAttrTc, kAttrTopk, kAttrTopkCluster, kAttrSlots };
+enum AttrSlot { kAttrCombine = 0, kAttrTc, kAttrTcLong, kAttrTopk, kAttrTopkCluster, kAttrSlots };
 cudaError_t set_smem_once(const void *kernel, int bytes, AttrSlot slot);
 
 int combine_table_bits(int topk_width);
