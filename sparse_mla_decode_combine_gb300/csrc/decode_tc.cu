@@ -484,8 +484,8 @@ __device__ __forceinline__ unsigned hash_insert(unsigned long long *tab, int bit
     }
 }
 
-// kRide: the next block's entries are loaded chunk by chunk during the dequant (worth it when a CTA
-// runs many blocks), instead of in one burst after it.
+// kRide: the next block's entries are loaded during the dequant, each chunk group's pieces once the
+// group is written (worth it when a CTA runs many blocks), instead of in one burst after it.
 template <bool kRide>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeParams p)
 {
@@ -878,12 +878,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                         st_shared_v4(cb + ((((uint32_t)qtr + 4u) ^ x7) << 4), pre[9].x, pre[9].y, pre[9].z,
                                      pre[9].w);
                     }
-                    if (kRide && ok_next) {   // the next block's pieces of this chunk take the registers just used
-                        if (c < 8) {
-                            pre[c] = ld_stream(enext + 64 * c + 16 * qtr);
-                        } else {
-                            pre[8] = ld_stream(enext + kRopeOffset + 16 * qtr);
-                            pre[9] = ld_stream(enext + kRopeOffset + 64 + 16 * qtr);
+                    if (kRide && ok_next && (c == 5 || c == 8)) {
+                        // once a chunk group is written, the next block's pieces of that group take its
+                        // registers (chunks 0-5, then 6-8)
+#pragma unroll
+                        for (int cc = 0; cc < kChunks; ++cc) {
+                            if (cc > c || (c == 8 && cc < 6))
+                                continue;
+                            if (cc < 8) {
+                                pre[cc] = ld_stream(enext + 64 * cc + 16 * qtr);
+                            } else {
+                                pre[8] = ld_stream(enext + kRopeOffset + 16 * qtr);
+                                pre[9] = ld_stream(enext + kRopeOffset + 64 + 16 * qtr);
+                            }
                         }
                     }
                     if (c == 5 || c == kChunks - 1) {
