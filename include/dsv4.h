@@ -359,6 +359,51 @@ DSV4_API dsv4_status dsv4_sparse_mla_decode_noalloc(const void *q, int64_t q_tok
                                                    float *lse, dsv4_stream_t stream);
 
 /*
+ * dsv4_sparse_mla_decode_mtp_union -- dsv4_sparse_mla_decode for speculative-verify batches in
+ * which the two query tokens of a request run in one tile over the union of their key lists.
+ *
+ * Source: "[ROCm] [DSv4] [Perf] Support DeepSeek v4 MTP" (vllm #43385), 风险 1 (MTP throughput
+ * falls at high concurrency because each request's tokens gather their keys separately); the
+ * per-token result is that of dsv4_sparse_mla_decode.
+ *
+ * Computes exactly what dsv4_sparse_mla_decode computes for the same arguments (up to the
+ * order in which a token's keys are summed), with this batch layout: num_tokens is even and
+ * tokens 2r and 2r + 1 are the two query tokens of request r, which share a block-table row
+ * (req_idx[2r] == req_idx[2r + 1]).  Each CTA takes 32 heads of both tokens (64 tile columns)
+ * and the union of the two tokens' combined lists, each key masked for the token that does not
+ * list it; a CTA of dsv4_sparse_mla_decode takes 64 heads of one token.
+ *
+ * Arguments: those of dsv4_sparse_mla_decode, with
+ *   req_idx         required (not NULL);
+ *   num_tokens      even, >= 0;
+ *   num_heads       32, 64 or 128 (others: DSV4_ERR_UNSUPPORTED);
+ *   num_blocks * page_block < 2^29;
+ *   workspace       at least dsv4_sparse_mla_decode_mtp_union_workspace_size(...) bytes.
+ * A request whose two tokens name different block-table rows, or a position of 2^29 or more,
+ * is a data error (recorded in the status word; the request's outputs are then not defined).
+ * Enqueues the combine of every token, one union kernel (one CTA a request) and the decode
+ * kernel.  Returns the codes of dsv4_sparse_mla_decode.
+ */
+DSV4_API dsv4_status dsv4_sparse_mla_decode_mtp_union(const void *q, int64_t q_token_stride, const void *kv_cache,
+                                                     int32_t num_blocks, int32_t page_block,
+                                                     const int32_t *block_table, int64_t bt_stride,
+                                                     int32_t max_blocks, int32_t num_reqs, const int32_t *req_idx,
+                                                     const int32_t *topk_idx, int64_t topk_stride,
+                                                     int32_t topk_width, const int32_t *topk_lens,
+                                                     const int32_t *seq_lens, int32_t num_tokens, int32_t num_heads,
+                                                     int32_t window, const float *sink, float softmax_scale,
+                                                     void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                                     dsv4_stream_t stream);
+
+/*
+ * dsv4_sparse_mla_decode_mtp_union_workspace_size -- bytes of device workspace
+ * dsv4_sparse_mla_decode_mtp_union needs (0 for arguments it rejects); depends on the current
+ * device's multiprocessor count, as dsv4_sparse_mla_decode_workspace_size.
+ */
+DSV4_API size_t dsv4_sparse_mla_decode_mtp_union_workspace_size(int32_t num_tokens, int32_t num_heads,
+                                                               int32_t topk_width, int32_t window);
+
+/*
  * dsv4_get_device_status -- synchronise `stream`, then read and clear the current
  * device's sticky status word.
  *

@@ -32,7 +32,8 @@ STATUS_NAMES = {0: "DSV4_OK", 1: "DSV4_ERR_INVALID_ARG", 2: "DSV4_ERR_BAD_INDEX"
 EXPORTED = ("dsv4_combine_topk_swa_indices", "dsv4_combine_topk_swa_indices_compressed", "dsv4_topk_select",
             "dsv4_qnorm_rope_kv_insert", "dsv4_selftest_wait_timeout",
             "dsv4_sparse_mla_decode_workspace_size", "dsv4_sparse_mla_decode", "dsv4_sparse_mla_decode_trace",
-            "dsv4_sparse_mla_decode_noalloc", "dsv4_get_device_status")
+            "dsv4_sparse_mla_decode_noalloc", "dsv4_sparse_mla_decode_mtp_union",
+            "dsv4_sparse_mla_decode_mtp_union_workspace_size", "dsv4_get_device_status")
 
 
 class Dsv4Error(RuntimeError):
@@ -86,6 +87,11 @@ def load_library():
     lib.dsv4_sparse_mla_decode_noalloc.restype = ctypes.c_int
     lib.dsv4_sparse_mla_decode_noalloc.argtypes = [P, i64, P, i32, i32, P, i64, i32, i32, P, P, i64, i32, P, P, i32,
                                                    i32, i32, P, ctypes.c_float, P, P, P]
+    lib.dsv4_sparse_mla_decode_mtp_union.restype = ctypes.c_int
+    lib.dsv4_sparse_mla_decode_mtp_union.argtypes = [P, i64, P, i32, i32, P, i64, i32, i32, P, P, i64, i32, P, P, i32,
+                                                     i32, i32, P, ctypes.c_float, P, P, P, ctypes.c_size_t, P]
+    lib.dsv4_sparse_mla_decode_mtp_union_workspace_size.restype = ctypes.c_size_t
+    lib.dsv4_sparse_mla_decode_mtp_union_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.dsv4_get_device_status.restype = ctypes.c_int
     lib.dsv4_get_device_status.argtypes = [P]
     _lib = lib
@@ -303,6 +309,45 @@ def dsv4_sparse_mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, bloc
         int(window), _ptr(sink), float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream))
 
 
+def dsv4_sparse_mla_decode_mtp_union_workspace_size(num_tokens: int, num_heads: int, topk_width: int,
+                                                    window: int) -> int:
+    return int(load_library().dsv4_sparse_mla_decode_mtp_union_workspace_size(num_tokens, num_heads, topk_width,
+                                                                              window))
+
+
+def dsv4_sparse_mla_decode_mtp_union(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                                     req_idx: torch.Tensor, topk_idx: torch.Tensor,
+                                     topk_lens: Optional[torch.Tensor], seq_lens: torch.Tensor, window: int,
+                                     sink: Optional[torch.Tensor], softmax_scale: float, out: torch.Tensor,
+                                     lse: Optional[torch.Tensor], workspace: torch.Tensor, stream=None) -> int:
+    """dsv4_sparse_mla_decode for batches of two-token requests (tokens 2r, 2r + 1 share
+    req_idx[2r]) run over the union of each request's two key lists (see include/dsv4.h);
+    workspace uint8 [>= dsv4_sparse_mla_decode_mtp_union_workspace_size(...)]."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv_cache, torch.uint8, "kv_cache", 3)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(req_idx, torch.int32, "req_idx", 1)
+    _need(topk_idx, torch.int32, "topk_idx", 2)
+    _need(topk_lens, torch.int32, "topk_lens", 1)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(sink, torch.float32, "sink", 1)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(lse, torch.float32, "lse", 2)
+    _need(workspace, torch.uint8, "workspace", 1)
+    if q.stride(1) != 576 or not kv_cache.is_contiguous() or not out.is_contiguous():
+        raise ValueError("q heads must be contiguous rows of 576; kv_cache and out must be contiguous")
+    if kv_cache.shape[2] != 656:
+        raise ValueError("kv_cache entries must be 656 bytes")
+    T, H, _ = q.shape
+    K = topk_idx.shape[1]
+    return load_library().dsv4_sparse_mla_decode_mtp_union(
+        _ptr(q), q.stride(0), _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(block_table),
+        block_table.stride(0), block_table.shape[1], block_table.shape[0], _ptr(req_idx),
+        _ptr(topk_idx) if K > 0 else None, max(topk_idx.stride(0), K), K, _ptr(topk_lens), _ptr(seq_lens), T, H,
+        int(window), _ptr(sink), float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+
+
 def dsv4_get_device_status(stream=None) -> int:
     return int(load_library().dsv4_get_device_status(_stream(stream)))
 
@@ -312,6 +357,13 @@ def dsv4_get_device_status(stream=None) -> int:
 # ----------------------------------------------------------------------------
 def workspace_for(num_tokens: int, num_heads: int, topk_width: int, window: int, device=None) -> torch.Tensor:
     n = dsv4_sparse_mla_decode_workspace_size(num_tokens, num_heads, topk_width, window)
+    if n == 0:
+        raise Dsv4Error(DSV4_ERR_INVALID_ARG, "workspace size")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def workspace_for_mtp_union(num_tokens: int, num_heads: int, topk_width: int, window: int, device=None) -> torch.Tensor:
+    n = dsv4_sparse_mla_decode_mtp_union_workspace_size(num_tokens, num_heads, topk_width, window)
     if n == 0:
         raise Dsv4Error(DSV4_ERR_INVALID_ARG, "workspace size")
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")

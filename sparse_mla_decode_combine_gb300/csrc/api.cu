@@ -54,20 +54,27 @@ inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 
 constexpr int kMaxWindow = 1 << 24;
 
-bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sms, Plan *pl)
+// mtp_union: the plan of an MTP union call (units are a request's two tokens x 32 heads, over the
+// union of the two combined lists)
+bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sms, Plan *pl, bool mtp_union = false)
 {
     if (num_tokens < 0 || topk_width < 0 || topk_width > kMaxTopkWidth || window < 0 || window > kMaxWindow)
         return false;
     if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128)
         return false;
+    if (mtp_union && (num_heads == 16 || num_tokens % 2 != 0))
+        return false;
     Plan p{};
     // One tensor-core kernel, 64 heads per CTA (a group of 16 or 32 heads runs as a 64-head group
     // whose missing heads have zero queries and are never written), 128-key blocks, one CTA per SM.
-    p.heads_per_group = 64;
+    // Union calls: 32 heads of each of the request's two tokens per CTA.
+    p.heads_per_group = mtp_union ? 32 : 64;
     p.groups = (num_heads + p.heads_per_group - 1) / p.heads_per_group;
-    p.cw = topk_width + window;
+    p.list_w = topk_width + window;
+    p.cw = mtp_union ? 2 * p.list_w : p.list_w;
     const int tile = decode_tc_block_keys();
-    const long long units0 = (long long)(num_tokens > 0 ? num_tokens : 1) * p.groups;
+    const int units_t = mtp_union ? num_tokens / 2 : num_tokens;
+    const long long units0 = (long long)(units_t > 0 ? units_t : 1) * p.groups;
     // the splits of a token form one thread-block cluster (<= 8 CTAs)
     const int split_cap = decode_tc_max_splits();
     const int max_splits = std::max(1, std::min(split_cap, (p.cw + tile - 1) / tile));
@@ -105,6 +112,16 @@ bool make_plan(int num_tokens, int num_heads, int topk_width, int window, int sm
     off = align_up(off + sizeof(int32_t) * (size_t)num_tokens * (size_t)p.cw, 256);
     p.off_order = off;   // the units' launch order, when the call needs one
     off = align_up(off + sizeof(int32_t) * (size_t)num_tokens * (size_t)p.groups, 256);
+    if (mtp_union) {
+        p.off_lists = off;
+        off = align_up(off + sizeof(int32_t) * (size_t)num_tokens * (size_t)p.list_w, 256);
+        p.off_lens = off;
+        off = align_up(off + sizeof(int32_t) * (size_t)num_tokens, 256);
+        p.off_ulist = off;
+        off = align_up(off + sizeof(int32_t) * (size_t)(num_tokens / 2) * (size_t)p.cw, 256);
+        p.off_ulen = off;
+        off = align_up(off + sizeof(int32_t) * (size_t)(num_tokens / 2), 256);
+    }
     p.total = std::max<size_t>(off, 256);
     *pl = p;
     return true;
@@ -286,13 +303,17 @@ dsv4_status decode_call(const void *q, int64_t q_token_stride, const void *kv_ca
                         int32_t topk_width, const int32_t *topk_lens, const int32_t *seq_lens, int32_t num_tokens,
                         int32_t num_heads, int32_t window, const float *sink, float softmax_scale, void *out,
                         float *lse, void *workspace, size_t workspace_bytes, int32_t *trace, int64_t trace_stride,
-                        int32_t *trace_lens, dsv4_stream_t stream)
+                        int32_t *trace_lens, dsv4_stream_t stream, bool mtp_union = false)
 {
     dsv4_status st = check_combine_args(topk_idx, topk_stride, topk_width, seq_lens, num_tokens, window);
     if (st != DSV4_OK)
         return st;
     if (num_heads != 16 && num_heads != 32 && num_heads != 64 && num_heads != 128)
         return DSV4_ERR_UNSUPPORTED;
+    if (mtp_union && num_heads == 16)
+        return DSV4_ERR_UNSUPPORTED;
+    if (mtp_union && (num_tokens % 2 != 0 || req_idx == nullptr))
+        return DSV4_ERR_INVALID_ARG;
     if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)   // the kernel's running max is taken on raw dot products
         return DSV4_ERR_INVALID_ARG;
     if (num_tokens == 0)
@@ -307,6 +328,8 @@ dsv4_status decode_call(const void *q, int64_t q_token_stride, const void *kv_ca
         return DSV4_ERR_INVALID_ARG;
     if ((long long)max_blocks * page_block > INT_MAX || (long long)num_blocks * page_block > INT_MAX)
         return DSV4_ERR_INVALID_ARG;
+    if (mtp_union && (long long)num_blocks * page_block >= (1LL << 29))   // cache slots carry two mask bits above them
+        return DSV4_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(workspace, 256))
         return DSV4_ERR_INVALID_ARG;
 
@@ -315,12 +338,25 @@ dsv4_status decode_call(const void *q, int64_t q_token_stride, const void *kv_ca
     if (device_info(&status, &sms) != cudaSuccess)
         return DSV4_ERR_CUDA;
     Plan pl;
-    if (!make_plan(num_tokens, num_heads, topk_width, window, sms, &pl))
+    if (!make_plan(num_tokens, num_heads, topk_width, window, sms, &pl, mtp_union))
         return DSV4_ERR_INVALID_ARG;
     if (workspace_bytes < pl.total)
         return DSV4_ERR_INVALID_ARG;
 
     char *ws = static_cast<char *>(workspace);
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (mtp_union) {   // every token's combined list, then each request's union list
+        int32_t *lists = reinterpret_cast<int32_t *>(ws + pl.off_lists);
+        int32_t *lens = reinterpret_cast<int32_t *>(ws + pl.off_lens);
+        cudaError_t e = launch_combine(topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens, window, lists,
+                                       pl.list_w, pl.list_w, lens, combine_table_bits(topk_width), cs);
+        if (e == cudaSuccess)
+            e = launch_mtp_union(lists, pl.list_w, lens, seq_lens, window, req_idx, num_tokens / 2,
+                                 reinterpret_cast<int32_t *>(ws + pl.off_ulist), pl.cw,
+                                 reinterpret_cast<int32_t *>(ws + pl.off_ulen), topk_width, status, cs);
+        if (e != cudaSuccess)
+            return DSV4_ERR_CUDA;
+    }
     DecodeParams p{};
     p.q = static_cast<const uint16_t *>(q);
     p.q_token_stride = q_token_stride;
@@ -359,11 +395,19 @@ dsv4_status decode_call(const void *q, int64_t q_token_stride, const void *kv_ca
     // units start longest first (a one-CTA ordering kernel runs ahead of the decode).  Equal
     // lengths gain nothing from it.
     p.order = nullptr;
-    if (topk_lens != nullptr && (long long)num_tokens * pl.groups > sms)
+    if (!mtp_union && topk_lens != nullptr && (long long)num_tokens * pl.groups > sms)
         p.order = reinterpret_cast<int32_t *>(ws + pl.off_order);
+    p.ulist = nullptr;
+    p.ulist_stride = 0;
+    p.ulen = nullptr;
+    if (mtp_union) {
+        p.ulist = reinterpret_cast<const int32_t *>(ws + pl.off_ulist);
+        p.ulist_stride = pl.cw;
+        p.ulen = reinterpret_cast<const int32_t *>(ws + pl.off_ulen);
+    }
 
     // one launch: the kernel combines, decodes and merges its splits
-    const cudaError_t e = launch_decode_tc(p, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_decode_tc(p, cs);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
@@ -399,6 +443,31 @@ extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode_trace(
                        num_reqs, req_idx, topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens,
                        num_heads, window, sink, softmax_scale, out, lse, workspace, workspace_bytes, combined,
                        combined_stride, combined_lens, stream);
+}
+
+extern "C" DSV4_API dsv4_status dsv4_sparse_mla_decode_mtp_union(
+    const void *q, int64_t q_token_stride, const void *kv_cache, int32_t num_blocks, int32_t page_block,
+    const int32_t *block_table, int64_t bt_stride, int32_t max_blocks, int32_t num_reqs, const int32_t *req_idx,
+    const int32_t *topk_idx, int64_t topk_stride, int32_t topk_width, const int32_t *topk_lens,
+    const int32_t *seq_lens, int32_t num_tokens, int32_t num_heads, int32_t window, const float *sink,
+    float softmax_scale, void *out, float *lse, void *workspace, size_t workspace_bytes, dsv4_stream_t stream)
+{
+    return decode_call(q, q_token_stride, kv_cache, num_blocks, page_block, block_table, bt_stride, max_blocks,
+                       num_reqs, req_idx, topk_idx, topk_stride, topk_width, topk_lens, seq_lens, num_tokens,
+                       num_heads, window, sink, softmax_scale, out, lse, workspace, workspace_bytes, nullptr, 0,
+                       nullptr, stream, true);
+}
+
+extern "C" DSV4_API size_t dsv4_sparse_mla_decode_mtp_union_workspace_size(int32_t num_tokens, int32_t num_heads,
+                                                                          int32_t topk_width, int32_t window)
+{
+    int sms = 0;
+    if (device_info(nullptr, &sms) != cudaSuccess)
+        return 0;
+    Plan pl;
+    if (!make_plan(num_tokens, num_heads, topk_width, window, sms, &pl, true))
+        return 0;
+    return pl.total;
 }
 
 extern "C" DSV4_API dsv4_status dsv4_get_device_status(dsv4_stream_t stream)

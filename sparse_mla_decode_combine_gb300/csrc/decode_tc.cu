@@ -82,6 +82,11 @@ constexpr uint32_t kColSb = 384;         // S^T over column chunks 5-8: 64 colum
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int kMaxSplits = 8;            // portable cluster size
+// MTP union lists: a position below 2^29, bit 29 set when the request's first token lists it,
+// bit 30 when its second does; the union kernel writes them and cache slots (below 2^29 as
+// well) carry the same bits through the decode
+constexpr int kUnionMaskShift = 29;
+constexpr int kUnionPosMask = (1 << kUnionMaskShift) - 1;
 
 // small shared region (after Q and the K tile)
 constexpr int kOffSlots = 0;             // int [3][128]: cache slots of blocks b, b+1, b+2
@@ -361,13 +366,16 @@ __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b)
 //   m = max(max_s m_s, sink), Z = sum_s l_s e^{m_s - m} + e^{sink - m},
 //   out = sum_s e^{m_s - m} O_s / Z  (BF16),  lse = m + ln Z,
 // skipping splits without keys (weight 0, whatever their slots hold).
+// kUnion: column c of the tile is head h0 + c % 32 of token t + c / 32 (MTP union calls); else
+// head h0 + c of token t.
+template <bool kUnion>
 __device__ __noinline__ void cluster_merge_local(uint16_t *out, float *lse, const float *sink, int num_heads, int S,
                                                  int t, int h0, int rank, const float *recv, const float *stat,
                                                  float *wts)
 {
     const int hp = (kNH + S - 1) / S;
     const int hb = rank * hp;
-    const int nh = max(0, min(min(kNH, num_heads - h0), hb + hp) - hb);   // owned heads that exist
+    const int nh = max(0, min(kUnion ? kNH : min(kNH, num_heads - h0), hb + hp) - hb);   // owned heads that exist
     const int tid = threadIdx.x;
     if (tid < nh) {
         const int h = hb + tid;
@@ -377,7 +385,7 @@ __device__ __noinline__ void cluster_merge_local(uint16_t *out, float *lse, cons
         const float mk = m;
         float sk = 0.f;
         if (sink != nullptr) {
-            sk = sink[h0 + h];
+            sk = sink[kUnion ? h0 + (h & 31) : h0 + h];
             m = fmaxf(m, sk);
         }
         float z = 0.f;
@@ -413,10 +421,12 @@ __device__ __noinline__ void cluster_merge_local(uint16_t *out, float *lse, cons
         uint2 o;
         o.x = pack_bf16x2(acc.x, acc.y);
         o.y = pack_bf16x2(acc.z, acc.w);
-        const int h = h0 + hb + hl;
-        *reinterpret_cast<uint2 *>(out + ((int64_t)t * num_heads + h) * kLatent + 4 * c) = o;
+        const int col = hb + hl;
+        const int64_t row = kUnion ? (int64_t)(t + (col >> 5)) * num_heads + h0 + (col & 31)
+                                   : (int64_t)t * num_heads + h0 + col;
+        *reinterpret_cast<uint2 *>(out + row * kLatent + 4 * c) = o;
         if (c == 0 && lse != nullptr)
-            lse[(int64_t)t * num_heads + h] = wts[hl * 10 + 8];
+            lse[row] = wts[hl * 10 + 8];
     }
 }
 
@@ -486,7 +496,10 @@ __device__ __forceinline__ unsigned hash_insert(unsigned long long *tab, int bit
 
 // kRide: the next block's entries are loaded during the dequant, each chunk group's pieces once the
 // group is written (worth it when a CTA runs many blocks), instead of in one burst after it.
-template <bool kRide>
+// kUnion: an MTP union call (unit = request and 32-head group; column c of the tile is head
+// h0 + c % 32 of token t + c / 32, t = 2 * request; keys come from the request's union list,
+// each masked for the token that does not list it).
+template <bool kRide, bool kUnion>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -559,16 +572,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
     const int cl = blockIdx.x / p.splits;
     const int unit = p.order != nullptr ? p.order[cl] : cl;
     const int group = unit % p.groups;
-    const int t = unit / p.groups;
-    const int h0 = group * kNH;
-    const int nhv = min(kNH, p.num_heads - h0);   // heads of the group that exist (16 or 32 heads: the rest are zero)
+    const int t = kUnion ? 2 * (unit / p.groups) : unit / p.groups;
+    const int h0 = group * (kUnion ? kNH / 2 : kNH);
+    // heads of the group that exist (16 or 32 heads: the rest are zero); all 64 columns in union calls
+    const int nhv = kUnion ? kNH : min(kNH, p.num_heads - h0);
+    // output row of tile column c
+    auto out_row = [&](int c) -> int64_t {
+        return kUnion ? (int64_t)(t + (c >> 5)) * p.num_heads + h0 + (c & 31) : (int64_t)t * p.num_heads + h0 + c;
+    };
 
     // ---- early loads: the token's sizes and top-k run first (the combine waits on them), then Q,
     // copied asynchronously into its tile (the combine works in the K tile region)
-    const int seq_len = p.seq_lens[t];
+    const int seq_len = kUnion ? 0 : p.seq_lens[t];   // union calls take their keys from the union list
     const int W = p.topk_width;
-    int n = W;
-    if (p.topk_lens != nullptr) {
+    int n = kUnion ? 0 : W;
+    if (!kUnion && p.topk_lens != nullptr) {
         n = p.topk_lens[t];
         n = n < 0 ? 0 : (n > W ? W : n);
     }
@@ -594,9 +612,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             const int i = wid + kWorkers * j;
             const int h = i / (kDim / 8);
             const int c = i % (kDim / 8);
-            cp_async16(sQ + (c >> 3) * kQChunkBytes + sw128(h, c & 7),
-                       p.q + (int64_t)t * p.q_token_stride + (int64_t)(h0 + min(h, nhv - 1)) * kDim + 8 * c,
-                       h < nhv ? 16u : 0u);
+            if constexpr (kUnion)
+                cp_async16(sQ + (c >> 3) * kQChunkBytes + sw128(h, c & 7),
+                           p.q + (int64_t)(t + (h >> 5)) * p.q_token_stride + (int64_t)(h0 + (h & 31)) * kDim + 8 * c,
+                           16u);
+            else
+                cp_async16(sQ + (c >> 3) * kQChunkBytes + sw128(h, c & 7),
+                           p.q + (int64_t)t * p.q_token_stride + (int64_t)(h0 + min(h, nhv - 1)) * kDim + 8 * c,
+                           h < nhv ? 16u : 0u);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
@@ -696,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             __syncthreads();   // wsum is rewritten by the next group of passes
     }
 
-    const int L = total + swa;
+    const int L = kUnion ? max(0, min(p.ulen[t >> 1], p.cw)) : total + swa;
     const int kend = min(L, klim);
     const int nkeys = max(0, kend - kbeg);
     const int nblocks = (nkeys + kBK - 1) / kBK;
@@ -708,7 +731,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         if (split == 0 && tid == 0)
             p.trace_lens[t] = L;
     }
-    if (row_ok) {   // the window part of this split
+    if (kUnion && row_ok) {   // this split's part of the request's union list: slots carry the token masks
+        const int32_t *urow = p.ulist + (int64_t)(t >> 1) * p.ulist_stride;
+        for (int i = kbeg + tid; i < kend; i += kThreads) {
+            const int e = urow[i];
+            const int pos_e = e & kUnionPosMask;
+            int sl = e >= 0 ? slot_of_position(p, row, pos_e, bt_s, bt_cached) : -1;
+            sl = sl >= 0 ? (sl | (((e >> kUnionMaskShift) & 3) << kUnionMaskShift)) : -1;
+            if (i - kbeg < kHeadSlots) {
+                slots[i - kbeg] = sl;
+                if (sl >= 0 && bt_cached)
+                    prefetch_entry(p, pos_e, bt_s);
+            } else {
+                slot_row[i] = sl;
+            }
+        }
+    } else if (row_ok) {   // the window part of this split
         for (int i = max(kbeg, total) + tid; i < kend; i += kThreads) {
             const int sl = slot_of_position(p, row, win_lo + (i - total), bt_s, bt_cached);
             if (i - kbeg < kHeadSlots)
@@ -727,12 +765,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         }
         if (p.splits == 1) {   // zero output, LSE from the sink alone
             if (tid < nhv && p.lse)
-                p.lse[(int64_t)t * p.num_heads + h0 + tid] = p.sink ? p.sink[h0 + tid] : -INFINITY;
+                p.lse[kUnion ? out_row(tid) : (int64_t)t * p.num_heads + h0 + tid] =
+                    p.sink ? p.sink[kUnion ? h0 + (tid & 31) : h0 + tid] : -INFINITY;
             for (int i = tid; i < nhv * kLatent / 8; i += kThreads) {
                 const int h = i / (kLatent / 8);
                 const int d = i % (kLatent / 8);
-                *reinterpret_cast<uint4 *>(p.out + ((int64_t)t * p.num_heads + h0 + h) * kLatent + 8 * d) =
-                    make_uint4(0, 0, 0, 0);
+                const int64_t orow = kUnion ? out_row(h) : (int64_t)t * p.num_heads + h0 + h;
+                *reinterpret_cast<uint4 *>(p.out + orow * kLatent + 8 * d) = make_uint4(0, 0, 0, 0);
             }
             return;
         }
@@ -740,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         if (tid < kNH)    // an empty partial: weight 0 in the merge, its O is never read
             push_stat(smem_u32(gbase), p.splits, split, tid, -INFINITY, 0.f);
         cluster_sync();   // every partial has landed
-        cluster_merge_local(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split,
+        cluster_merge_local<kUnion>(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split,
                             reinterpret_cast<const float *>(gbase + kQBytes), reinterpret_cast<const float *>(gbase),
                             reinterpret_cast<float *>(gbase + 1024));
         return;
@@ -834,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             const int sidx = slots[(b % 3) * kBK + rrow];
             pre_ok = sidx >= 0;
             if (pre_ok) {
-                const uint8_t *e = p.kv + (int64_t)sidx * kEntryBytes;
+                const uint8_t *e = p.kv + (int64_t)(kUnion ? sidx & kUnionPosMask : sidx) * kEntryBytes;
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     pre[c] = ld_stream(e + 64 * c + 16 * qtr);
@@ -863,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                     if (kRide && c == 0 && b + 1 < nblocks) {   // (after the first wait: the slots of b + 1 are visible)
                         const int sidx = slots[((b + 1) % 3) * kBK + rrow];
                         ok_next = sidx >= 0;
-                        enext = p.kv + (int64_t)max(sidx, 0) * kEntryBytes;
+                        enext = p.kv + (int64_t)(ok_next ? (kUnion ? sidx & kUnionPosMask : sidx) : 0) * kEntryBytes;
                     }
                     const uint32_t cb = rb + (uint32_t)c * kChunkBytes;
                     if (!pre_ok) {
@@ -922,7 +961,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             // ---- softmax of block b: this warp's 32 keys (TMEM lanes) x 16 heads
             mbar_wait(bar_s, ph, flags, p.status);
             tc_after();
-            const bool kv = (b * kBK + key < nkeys) && slots[(b % 3) * kBK + key] >= 0;
+            bool kv;
+            if constexpr (kUnion) {   // warps 1-8 hold the first token's heads, 9-16 the second's
+                const int ksl = slots[(b % 3) * kBK + key];
+                kv = (b * kBK + key < nkeys) && ksl >= 0 && ((ksl >> (kUnionMaskShift + ((warp - 1) >> 3))) & 1);
+            } else {
+                kv = (b * kBK + key < nkeys) && slots[(b % 3) * kBK + key] >= 0;
+            }
             float *redb = red + (b & 1) * 4 * kNH;
             {   // per-head maxima over this warp's keys; lane j keeps head hs + j
                 float mine = -INFINITY;
@@ -1017,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
             // warm L2 for block b + 2 (its register loads are issued in block b + 1), after the hand-off
             // of P: the issuing thread waits on the prefetch
             if (lane < 8 && b + 2 < nblocks && next_slot >= 0)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.kv + (int64_t)next_slot * kEntryBytes),
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.kv + (int64_t)(kUnion ? next_slot & kUnionPosMask : next_slot) * kEntryBytes),
                              "r"((uint32_t)kEntryBytes) : "memory");
         }
 
@@ -1078,13 +1123,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
                 float M = ms;
                 float Z = lsum;
                 if (p.sink != nullptr && h < nhv) {
-                    const float sk = p.sink[h0 + h];
+                    const float sk = p.sink[kUnion ? h0 + (h & 31) : h0 + h];
                     M = fmaxf(ms, sk);
                     Z = (ms == -INFINITY ? 0.f : lsum * expf(ms - M)) + expf(sk - M);
                 }
                 fin[h] = (Z > 0.f && ms != -INFINITY) ? expf(ms - M) / Z : 0.f;
                 if (p.lse && h < nhv)
-                    p.lse[(int64_t)t * p.num_heads + h0 + h] = Z > 0.f ? M + logf(Z) : -INFINITY;
+                    p.lse[kUnion ? out_row(h) : (int64_t)t * p.num_heads + h0 + h] = Z > 0.f ? M + logf(Z) : -INFINITY;
             } else {
                 alpha[h] = ms;
                 fin[h] = ms == -INFINITY ? 0.f : lsum;
@@ -1106,8 +1151,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int h = hs + j;
-                    if (h < nhv)
-                        p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] = bf16_bits(__uint_as_float(x[j]) * fin[h]);
+                    if (h < nhv) {
+                        if constexpr (kUnion)
+                            p.out[out_row(h) * kLatent + dv] = bf16_bits(__uint_as_float(x[j]) * fin[h]);
+                        else
+                            p.out[((int64_t)t * p.num_heads + h0 + h) * kLatent + dv] =
+                                bf16_bits(__uint_as_float(x[j]) * fin[h]);
+                    }
                 }
             }
         }
@@ -1119,7 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         if (is_worker) {
             const int S = p.splits;
             const int hp = (kNH + S - 1) / S;
-            const int nhe = min(kNH, p.num_heads - h0);   // the merge reads only the heads that exist
+            const int nhe = kUnion ? kNH : min(kNH, p.num_heads - h0);   // the merge reads only the heads that exist
             if (wid < nhe)
                 push_stat(smem_u32(gbase), S, split, wid, alpha[wid], fin[wid]);
             const uint32_t recv_s = sK;
@@ -1152,7 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecodePara
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     if (p.splits > 1) {
         cluster_sync();   // every partial has landed
-        cluster_merge_local(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split,
+        cluster_merge_local<kUnion>(p.out, p.lse, p.sink, p.num_heads, p.splits, t, h0, split,
                             reinterpret_cast<const float *>(gbase + kQBytes), reinterpret_cast<const float *>(gbase),
                             reinterpret_cast<float *>(gbase + 1024));
     }
@@ -1257,7 +1307,7 @@ int decode_tc_resident_ctas(int splits)
         return 0;
     if (cache[dev][splits] > 0)
         return cache[dev][splits];
-    if (set_smem_once(reinterpret_cast<const void *>(decode_tc_kernel<false>), kSmemBytes, kAttrTc) != cudaSuccess)
+    if (set_smem_once(reinterpret_cast<const void *>(decode_tc_kernel<false, false>), kSmemBytes, kAttrTc) != cudaSuccess)
         return 0;
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1275,7 +1325,7 @@ int decode_tc_resident_ctas(int splits)
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(decode_tc_kernel<false>), &cfg) !=
+        if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(decode_tc_kernel<false, false>), &cfg) !=
             cudaSuccess) {
             cudaGetLastError();
             return 0;
@@ -1298,14 +1348,25 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
 {
     if (p.num_tokens <= 0)
         return cudaSuccess;
-    if (p.heads_per_group != kNH || p.num_heads < 1 || p.chunk <= 0 || p.splits < 1 || p.splits > kMaxSplits || p.topk_width < 0 ||
+    if (p.heads_per_group != (p.ulist != nullptr ? kNH / 2 : kNH) || (p.ulist != nullptr && p.order != nullptr) ||
+        p.num_heads < 1 || p.chunk <= 0 || p.splits < 1 || p.splits > kMaxSplits || p.topk_width < 0 ||
         p.topk_width > kMaxTopkWidth || p.table_bits < 1 || p.table_bits > kHashBitsMax)
         return cudaErrorInvalidValue;
     // CTAs of more than three blocks load the next block's entries during the dequant
     const bool ride = p.chunk > 3 * kBK;
-    const void *kernel = ride ? reinterpret_cast<const void *>(decode_tc_kernel<true>)
-                              : reinterpret_cast<const void *>(decode_tc_kernel<false>);
-    cudaError_t e = set_smem_once(kernel, kSmemBytes, ride ? kAttrTcLong : kAttrTc);
+    const bool uni = p.ulist != nullptr;
+    const void *kernel;
+    AttrSlot slot;
+    if (uni) {
+        kernel = ride ? reinterpret_cast<const void *>(decode_tc_kernel<true, true>)
+                      : reinterpret_cast<const void *>(decode_tc_kernel<false, true>);
+        slot = ride ? kAttrTcUnionLong : kAttrTcUnion;
+    } else {
+        kernel = ride ? reinterpret_cast<const void *>(decode_tc_kernel<true, false>)
+                      : reinterpret_cast<const void *>(decode_tc_kernel<false, false>);
+        slot = ride ? kAttrTcLong : kAttrTc;
+    }
+    cudaError_t e = set_smem_once(kernel, kSmemBytes, slot);
     if (e != cudaSuccess)
         return e;
     if (p.order != nullptr) {   // the launch order, ahead of the decode (which waits for it)
@@ -1323,7 +1384,9 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
         if (e != cudaSuccess)
             return e;
     }
-    const long long grid = (long long)p.num_tokens * p.groups * p.splits;
+    // units: (token, 64-head group), or (request, 32-head group) in union calls
+    const long long units = p.ulist != nullptr ? (long long)(p.num_tokens / 2) * p.groups : (long long)p.num_tokens * p.groups;
+    const long long grid = units * p.splits;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);

@@ -34,6 +34,10 @@ struct Plan {
     int cw;                // row width of the workspace's slot rows (topk_width + window)
     int combine_table_bits;
     size_t off_combined, off_order, total;
+    // MTP union calls: the tokens' combined lists [T, list_w] and lengths, the requests' union
+    // lists [T / 2, cw] and lengths
+    int list_w;
+    size_t off_lists, off_lens, off_ulist, off_ulen;
 };
 
 struct DecodeParams {
@@ -76,16 +80,27 @@ struct DecodeParams {
     // launch order of the (token, head group) units, longest estimated list first, written by
     // the ordering kernel ahead of the decode; null: index order
     int32_t *order;
+    // MTP union calls: the two tokens of request r (2r, 2r + 1) share one CTA per 32 heads and the
+    // union list of row r (positions with bit 29 set for token 2r's keys, bit 30 for token
+    // 2r + 1's), ulen[r] entries; null in other calls
+    const int32_t *ulist;
+    int64_t ulist_stride;
+    const int32_t *ulen;
 };
 
 // Raises a kernel's dynamic shared-memory limit to at least `bytes`, once per
 // (device, kernel slot); later calls with no larger size touch no CUDA state, so a
 // call made after the first one on a device is safe inside stream capture.
-enum AttrSlot { kAttrCombine = 0, kAttrTc, kAttrTcLong, kAttrTopk, kAttrTopkCluster, kAttrSlots };
+enum AttrSlot { kAttrCombine = 0, kAttrTc, kAttrTcLong, kAttrTcUnion, kAttrTcUnionLong, kAttrUnion, kAttrTopk,
+                kAttrTopkCluster, kAttrSlots };
 cudaError_t set_smem_once(const void *kernel, int bytes, AttrSlot slot);
 
 int combine_table_bits(int topk_width);
 size_t combine_smem_bytes(int table_bits, int topk_width);
+// the union lists of MTP requests (tokens 2r, 2r + 1) from the tokens' combined lists
+cudaError_t launch_mtp_union(const int32_t *lists, int64_t lstride, const int32_t *lens, const int32_t *seq_lens,
+                             int window, const int32_t *req_idx, int num_reqs, int32_t *ulist, int64_t ustride,
+                             int32_t *ulen, int topk_width, unsigned *status, cudaStream_t stream);
 cudaError_t launch_combine(const int32_t *topk, int64_t topk_stride, int topk_width, const int32_t *topk_lens,
                            const int32_t *seq_lens, int num_tokens, int window, int32_t *combined,
                            int64_t combined_stride, int combined_width, int32_t *combined_lens, int table_bits,

@@ -102,3 +102,22 @@ def test_host_side_argument_errors(lib):
     bad = list(args)
     bad[15] = 0
     assert lib.dsv4_sparse_mla_decode(*bad) == pkg.DSV4_OK   # nothing to do
+    # MTP union decode: 16 heads, an odd token count, no req_idx; nothing to do
+    un = lib.dsv4_sparse_mla_decode_mtp_union
+    uargs = list(args)
+    uargs[9] = ctypes.c_void_p(16)   # req_idx
+    uargs[15] = 2                    # two tokens: one request
+    uargs[16] = 32
+    bad = list(uargs)
+    bad[16] = 16
+    assert un(*bad) == pkg.DSV4_ERR_UNSUPPORTED
+    bad = list(uargs)
+    bad[15] = 3
+    assert un(*bad) == pkg.DSV4_ERR_INVALID_ARG
+    bad = list(uargs)
+    bad[9] = None
+    assert un(*bad) == pkg.DSV4_ERR_INVALID_ARG
+    bad = list(uargs)
+    bad[15] = 0
+    assert un(*bad) == pkg.DSV4_OK
+    assert lib.dsv4_sparse_mla_decode_mtp_union_workspace_size(3, 64, 64, 8) == 0   # odd token count
