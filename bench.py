@@ -68,7 +68,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="time only --workload (the default line also times all five decode workloads)")
-    ap.add_argument("--op", choices=["decode", "combine-compressed", "topk-select", "qnorm-rope-insert"],
+    ap.add_argument("--op", choices=["decode", "combine-compressed", "topk-select", "qnorm-rope-insert", "mtp-union"],
                     default="decode", help="decode (the headline), or one of the steps around it on its own")
     ap.add_argument("--topk-workload", choices=["long-batch", "long-decode"], default="long-batch",
                     help="top-k selection workload (synth.topk_config)")
@@ -316,9 +316,10 @@ class DecodeBench:
     block tables, queries, outputs), so that the bytes gathered over one rotation exceed 4x the
     L2; steps replayed from CUDA graphs, CUDA events on the launching stream."""
 
-    def __init__(self, pkg, w, dev, replicas=0):
+    def __init__(self, pkg, w, dev, replicas=0, mtp_union=False):
         import torch
         self.pkg, self.w, self.dev = pkg, w, dev
+        self.mtp_union = mtp_union
         self.base = synth_to_device(w, dev)
         self.T, self.H, self.K, self.W = w.num_tokens, w.num_heads, w.topk_width, w.window
         lens = combined_lengths(w)
@@ -345,15 +346,15 @@ class DecodeBench:
             self.outs.append(torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev))
             self.lses.append(torch.empty((T, H), dtype=torch.float32, device=dev))
         del self.base["kv_cache"]
-        self.ws = pkg.workspace_for(T, H, self.K, self.W, dev)
+        self.ws = (pkg.workspace_for_mtp_union if mtp_union else pkg.workspace_for)(T, H, self.K, self.W, dev)
         self.stream = torch.cuda.Stream(device=dev)
 
     def step(self, i, stream=None):
         r = i % self.R
         b = self.base
-        return self.pkg.dsv4_sparse_mla_decode(self.qs[r], self.pool, self.bts[r], b["req_idx"], b["topk_idx"],
-                                               b["topk_lens"], b["seq_lens"], self.W, b["sink"], b["softmax_scale"],
-                                               self.outs[r], self.lses[r], self.ws, stream=stream)
+        call = self.pkg.dsv4_sparse_mla_decode_mtp_union if self.mtp_union else self.pkg.dsv4_sparse_mla_decode
+        return call(self.qs[r], self.pool, self.bts[r], b["req_idx"], b["topk_idx"], b["topk_lens"], b["seq_lens"],
+                    self.W, b["sink"], b["softmax_scale"], self.outs[r], self.lses[r], self.ws, stream=stream)
 
     def time(self, steps, warmup, world=1, sampler=None):
         """Milliseconds for exactly `steps` steps (max over ranks) and the host times around them."""
@@ -703,6 +704,56 @@ def run_ours(args):
     return 0
 
 
+def run_mtp_union(args):
+    """The MTP union decode on the spec-verify workload (64 requests x 2 tokens x 128 heads), against
+    the plain decode on the same inputs, as synthesised (each token's top-k row drawn on its own) and
+    with 90 % of each draft token's picks shared with its partner. A step is one call; the union
+    call enqueues the combine, the union kernel and the decode."""
+    import torch
+    import synth
+    import sparse_mla_decode_combine_gb300 as pkg
+    from sparse_mla_decode_combine_gb300 import build as pkg_build
+    pkg_build.build()
+    pkg.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    sampler.start()
+    time.sleep(0.5)
+    w0 = synth.config(4)
+    rows = {}
+    for label, w in (("independent picks", w0), ("90% shared picks", synth.with_shared_picks(w0, 17, 0.9))):
+        for mode in ("union", "plain"):
+            bn = DecodeBench(pkg, w, dev, mtp_union=(mode == "union"))
+            msn, a0, a1 = bn.time(args.steps, args.warmup)
+            rl = bn.roofline(msn / 1e3 / args.steps)
+            rows[(label, mode)] = {"ms_per_step": msn / args.steps, "value": w.num_tokens * args.steps / (msn / 1e3),
+                                   "frac": rl["frac"], "clocks": sampler.summary(a0, a1), "bench": bn}
+            if not (label == "independent picks" and mode == "union"):
+                del bn
+                rows[(label, mode)].pop("bench")
+                torch.cuda.empty_cache()
+    head = rows[("independent picks", "union")]
+    bn = head.pop("bench")
+    rl = bn.roofline(head["ms_per_step"] / 1e3)
+    rl.update({"kernel": "decode_tc_kernel", "traffic": None,
+               "timed": "whole MTP union call per step (combine, union kernel, decode), CUDA events on the launching stream"})
+    config = workload_config(w0, {"l2": bn.l2_note(), "replicas": bn.R, "keys_per_step": bn.keys_per_step,
+                                  "call": "dsv4_sparse_mla_decode_mtp_union"})
+    del bn
+    torch.cuda.empty_cache()
+    sampler.stop()
+    line = {"op": "mtp-union", "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config, "roofline": rl,
+            "gpu_launches": 3 * args.steps, "launches_per_step": 3, "clocks": head["clocks"],
+            "comparison": {f"{label}, {mode}": {k: v for k, v in r.items() if k != "clocks"}
+                           for (label, mode), r in rows.items()}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_combine_compressed(args):
     """The compressed-region combine on its own: 64 requests x 4 tokens (speculative verify
     shape), top-k 2048 of a 4x-compressed region, window 128, rows of 2304 entries. Bytes per
@@ -980,6 +1031,10 @@ def main():
         if args.impl == "reference" or int(os.environ.get("RANK", "0")) != 0:
             return 0
         return run_combine_compressed(args)
+    if args.op == "mtp-union":
+        if args.impl == "reference" or int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        return run_mtp_union(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -316,6 +316,18 @@ def small_config(n: int) -> Workload:
     raise ValueError(n)
 
 
+def with_shared_picks(w: Workload, seed: int, keep: float) -> Workload:
+    """Two-token requests whose draft token's top-k row repeats most of its partner's: a fraction
+    `keep` of token 2r + 1's entries copied from token 2r's row (an indexer scores neighbouring
+    positions alike, so a request's two tokens pick mostly the same keys)."""
+    rng = np.random.default_rng(seed)
+    topk = w.topk_idx.copy()
+    for r in range(w.num_tokens // 2):
+        m = rng.random(topk.shape[1]) < keep
+        topk[2 * r + 1, m] = topk[2 * r, m]
+    return dataclasses.replace(w, name=f"{w.name}, draft picks {int(round(100 * keep))}% shared", topk_idx=topk)
+
+
 def to_device(w: Workload, device="cuda") -> dict:
     """Copy a workload's arrays into torch tensors on `device` (BF16 q, uint8 cache, int32 indices)."""
     import torch

@@ -34,14 +34,7 @@ def run_union(w: synth.Workload):
 
 
 def shared_picks(w: synth.Workload, seed: int, keep: float) -> synth.Workload:
-    """Token 2r + 1's top-k row made to repeat most of token 2r's (as a draft token's indexer
-    picks mostly the same keys): a fraction `keep` of its entries copied from its partner's row."""
-    rng = np.random.default_rng(seed)
-    topk = w.topk_idx.copy()
-    for r in range(w.num_tokens // 2):
-        m = rng.random(topk.shape[1]) < keep
-        topk[2 * r + 1, m] = topk[2 * r, m]
-    return dataclasses.replace(w, topk_idx=topk)
+    return synth.with_shared_picks(w, seed, keep)
 
 
 def mtp_workload(seed: int, heads: int, seqs, width: int, window: int, sink: bool, counts=None,
