@@ -708,7 +708,7 @@ def run_mtp_union(args):
     """The MTP union decode on the spec-verify workload (64 requests x 2 tokens x 128 heads), against
     the plain decode on the same inputs, as synthesised (each token's top-k row drawn on its own) and
     with 90 % of each draft token's picks shared with its partner. A step is one call; the union
-    call enqueues the combine, the union kernel and the decode."""
+    call enqueues the combine, the union kernel, the ordering kernel and the decode."""
     import torch
     import synth
     import sparse_mla_decode_combine_gb300 as pkg
@@ -734,11 +734,13 @@ def run_mtp_union(args):
                 del bn
                 rows[(label, mode)].pop("bench")
                 torch.cuda.empty_cache()
+    # combine, union lists, (ordering when the units outnumber the multiprocessors), decode
+    launches = 3 + (1 if (w0.num_tokens // 2) * (w0.num_heads // 32) > props.multi_processor_count else 0)
     head = rows[("independent picks", "union")]
     bn = head.pop("bench")
     rl = bn.roofline(head["ms_per_step"] / 1e3)
     rl.update({"kernel": "decode_tc_kernel", "traffic": None,
-               "timed": "whole MTP union call per step (combine, union kernel, decode), CUDA events on the launching stream"})
+               "timed": "whole MTP union call per step (combine, union kernel, ordering kernel, decode), CUDA events on the launching stream"})
     config = workload_config(w0, {"l2": bn.l2_note(), "replicas": bn.R, "keys_per_step": bn.keys_per_step,
                                   "call": "dsv4_sparse_mla_decode_mtp_union"})
     del bn
@@ -747,7 +749,7 @@ def run_mtp_union(args):
     line = {"op": "mtp-union", "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config, "roofline": rl,
-            "gpu_launches": 3 * args.steps, "launches_per_step": 3, "clocks": head["clocks"],
+            "gpu_launches": launches * args.steps, "launches_per_step": launches, "clocks": head["clocks"],
             "comparison": {f"{label}, {mode}": {k: v for k, v in r.items() if k != "clocks"}
                            for (label, mode), r in rows.items()}}
     print(json.dumps(line), flush=True)

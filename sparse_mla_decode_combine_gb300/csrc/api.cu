@@ -394,8 +394,10 @@ dsv4_status decode_call(const void *q, int64_t q_token_stride, const void *kv_ca
     // Lists of different lengths over more (token, head group) units than multiprocessors: the
     // units start longest first (a one-CTA ordering kernel runs ahead of the decode).  Equal
     // lengths gain nothing from it.
+    // (union calls: the union lists' lengths vary with the overlap of a request's two lists)
     p.order = nullptr;
-    if (!mtp_union && topk_lens != nullptr && (long long)num_tokens * pl.groups > sms)
+    if (mtp_union ? (long long)(num_tokens / 2) * pl.groups > sms
+                  : topk_lens != nullptr && (long long)num_tokens * pl.groups > sms)
         p.order = reinterpret_cast<int32_t *>(ws + pl.off_order);
     p.ulist = nullptr;
     p.ulist_stride = 0;

@@ -1229,10 +1229,17 @@ __device__ __forceinline__ int order_key(const int32_t *topk_lens, const int32_t
     return (int)(blocks < kOrderThreads - 1 ? blocks : kOrderThreads - 1);
 }
 
+// In MTP union calls (ulen not null) the units are (request, 32-head group) and the key is the
+// number of 128-key blocks of the request's union list.
 __global__ void __launch_bounds__(kOrderThreads) decode_order_kernel(const int32_t *topk_lens, const int32_t *seq_lens,
                                                                      int num_tokens, int topk_width, int window,
-                                                                     int groups, int32_t *order)
+                                                                     int groups, int32_t *order, const int32_t *ulen)
 {
+    auto key_of = [&](int u) -> int {
+        if (ulen != nullptr)
+            return min(kOrderThreads - 1, (max(ulen[u / groups], 0) + 127) / 128);
+        return order_key(topk_lens, seq_lens, u / groups, topk_width, window);
+    };
     __shared__ int cnt[kOrderThreads];
     __shared__ int wsum[kOrderThreads / 32];
     const int tid = threadIdx.x;
@@ -1242,7 +1249,7 @@ __global__ void __launch_bounds__(kOrderThreads) decode_order_kernel(const int32
     __syncthreads();
     const int units = num_tokens * groups;
     for (int u = tid; u < units; u += kOrderThreads)
-        atomicAdd(&cnt[order_key(topk_lens, seq_lens, u / groups, topk_width, window)], 1);
+        atomicAdd(&cnt[key_of(u)], 1);
     __syncthreads();
     // start[k] = number of units with a larger key: an inclusive scan of the counts in
     // descending key order (thread i holds key kOrderThreads - 1 - i), minus the own count
@@ -1266,7 +1273,7 @@ __global__ void __launch_bounds__(kOrderThreads) decode_order_kernel(const int32
     cnt[k] = before + v - c;
     __syncthreads();
     for (int u = tid; u < units; u += kOrderThreads)
-        order[atomicAdd(&cnt[order_key(topk_lens, seq_lens, u / groups, topk_width, window)], 1)] = u;
+        order[atomicAdd(&cnt[key_of(u)], 1)] = u;
 }
 
 // Self-test of the bounded waits: one thread waits, at most `limit` SM cycles, on an mbarrier
@@ -1348,8 +1355,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
 {
     if (p.num_tokens <= 0)
         return cudaSuccess;
-    if (p.heads_per_group != (p.ulist != nullptr ? kNH / 2 : kNH) || (p.ulist != nullptr && p.order != nullptr) ||
-        p.num_heads < 1 || p.chunk <= 0 || p.splits < 1 || p.splits > kMaxSplits || p.topk_width < 0 ||
+    if (p.heads_per_group != (p.ulist != nullptr ? kNH / 2 : kNH) || p.num_heads < 1 || p.chunk <= 0 || p.splits < 1 || p.splits > kMaxSplits || p.topk_width < 0 ||
         p.topk_width > kMaxTopkWidth || p.table_bits < 1 || p.table_bits > kHashBitsMax)
         return cudaErrorInvalidValue;
     // CTAs of more than three blocks load the next block's entries during the dequant
@@ -1379,8 +1385,9 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream)
         oattr[0].val.programmaticStreamSerializationAllowed = 1;
         ocfg.attrs = oattr;
         ocfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&ocfg, decode_order_kernel, p.topk_lens, p.seq_lens, p.num_tokens, p.topk_width,
-                               p.window, p.groups, p.order);
+        e = cudaLaunchKernelEx(&ocfg, decode_order_kernel, p.topk_lens, p.seq_lens,
+                               p.ulist != nullptr ? p.num_tokens / 2 : p.num_tokens, p.topk_width, p.window, p.groups,
+                               p.order, p.ulen);
         if (e != cudaSuccess)
             return e;
     }
